@@ -1,0 +1,512 @@
+#!/usr/bin/env python
+"""Benchmark of the ragged paged-attention hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch: the paged KV-append
+(cb_kv_append) followed by the ragged paged-attention pass (cb_ragged_paged_attention: planner,
+split-KV decode kernel, LSE merge, tcgen05 chunk kernel).  Default workload: the mixed ragged
+batch at max_batch_tokens = 2048 (120 decode tokens at prior context U[256, 8192] plus one
+1928-token chunk at prior context 3000; 32 query / 8 KV heads, head_dim 128, block size 32), the
+one batch of the named set in which every step of the path runs.
+
+Prints ONE JSON line.  `value` is query tokens per second of the whole job, from device time
+(CUDA events on the launching stream) with inputs resident in HBM; L2 is flushed (a 512 MiB
+write) before every timed step.  `e2e` is the same metric through the Python API with the step's
+inputs copied from pinned host memory and the output copied back inside the timed region.
+`roofline` is the dominant kernel's algorithmic bytes (or FLOPs) per launch over its average
+device time, measured by events the library records around each kernel.  `cpu_baseline` is the
+float64 oracle timed on a bounded sample of the same workload on this host's cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixed|decode|prefill|longtail]
+    python bench.py --impl reference ...     # the oracle as the reference arm
+Multi-GPU (torchrun): each rank runs an independent replica (the path shards by sequence with no
+exchange), timing is the max over ranks, and `value` sums all ranks' tokens ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s (% of HBM peak); mixed-batch query tokens/sec"
+WORKLOADS = {"tiny": 1, "decode": 2, "mixed": 3, "prefill": 4, "longtail": 5}
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["cb", "reference"], default="cb")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed")
+    p.add_argument("--decode-ctas", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------- workload facts
+
+def decode_kv_bytes(b: workloads.Batch):
+    """Algorithmic HBM bytes of the decode pass: every distinct K/V row a decode token reads
+    (shared prefix pages once), plus its q and out rows; and the same with sharing counted per
+    sequence ("logical")."""
+    q_lens = np.diff(b.cu_seqlens_q)
+    row_bytes = b.num_kv_heads * b.head_dim * 2 * 2          # K + V, bf16
+    slots = []
+    logical = 0
+    n_dec = 0
+    for s in np.nonzero(q_lens == 1)[0]:
+        kv = int(b.kv_lens[s])
+        j = np.arange(kv)
+        slots.append(b.block_table[s][j // b.block_size].astype(np.int64) * b.block_size
+                     + j % b.block_size)
+        logical += kv
+        n_dec += 1
+    unique = int(np.unique(np.concatenate(slots)).size) if slots else 0
+    qo = n_dec * b.num_q_heads * b.head_dim * 2 * 2
+    return unique * row_bytes + qo, logical * row_bytes + qo
+
+
+def chunk_flops(b: workloads.Batch):
+    """Algorithmic FLOPs of the chunk pass: 4 * D * Hq per unmasked (query, key) pair."""
+    q_lens = np.diff(b.cu_seqlens_q)
+    pairs = 0
+    for s in np.nonzero(q_lens > 1)[0]:
+        n = int(q_lens[s])
+        ctx = int(b.kv_lens[s]) - n
+        pairs += n * ctx + n * (n + 1) // 2
+    return 4.0 * b.head_dim * b.num_q_heads * pairs
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "continuous_batching_paged_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[f"{kernel}:{workload}"]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash(*rec.get("sources", [])):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = []
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                sm, smax, pw, util = float(parts[0]), float(parts[1]), float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            rows.append((sm, smax, pw, util, parts[4:]))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r[3] > 0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(busy),
+                "power_w_max": max(r[2] for r in busy)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "cb") else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def sub_batch(b: workloads.Batch, seqs, chunk_rows=None) -> workloads.Batch:
+    """The listed sequences of b as a batch of their own (a chunk keeps its prior context and
+    its first chunk_rows queries)."""
+    q_lens = np.diff(b.cu_seqlens_q)
+    new_q, new_kv, rows_q, rows_kv = [], [], [], []
+    for s in seqs:
+        n = int(q_lens[s])
+        ctx = int(b.kv_lens[s]) - n
+        if chunk_rows is not None and n > chunk_rows:
+            n = chunk_rows
+        c0 = int(b.cu_seqlens_q[s])
+        rows_q.append(b.q[c0:c0 + n])
+        rows_kv.append((b.k_new[c0:c0 + n], b.v_new[c0:c0 + n]))
+        new_q.append(n)
+        new_kv.append(ctx + n)
+    cu = np.zeros(len(seqs) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(new_q)
+    # Carry only the blocks the sampled sequences reference (same contents, renumbered).
+    table = b.block_table[list(seqs)].copy()
+    used = np.unique(table[table >= 0])
+    remap = np.full(b.num_pages, -1, dtype=np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    table = np.where(table >= 0, remap[np.maximum(table, 0)], -1).astype(np.int32)
+    return workloads.Batch(name=b.name + "-sample", q=np.concatenate(rows_q),
+                           k_new=np.concatenate([k for k, _ in rows_kv]),
+                           v_new=np.concatenate([v for _, v in rows_kv]),
+                           k_pages=b.k_pages[used], v_pages=b.v_pages[used],
+                           block_table=table, cu_seqlens_q=cu,
+                           kv_lens=np.asarray(new_kv, dtype=np.int32), block_size=b.block_size,
+                           scale=b.scale, num_q_heads=b.num_q_heads,
+                           num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
+
+
+def oracle_step(sb: workloads.Batch):
+    from oracle import paged_attention as opa
+    kp, vp = opa.kv_append(sb.k_new, sb.v_new, sb.k_pages, sb.v_pages, sb.block_table,
+                           sb.cu_seqlens_q, sb.kv_lens, sb.block_size)
+    opa.ragged_paged_attention(sb.q, kp, vp, sb.block_table, sb.cu_seqlens_q, sb.kv_lens,
+                               sb.block_size, sb.scale)
+
+
+def cpu_sample_plan(b: workloads.Batch, budget_s: float):
+    """A bounded sample: decode sequences and (for chunks) the first 128 queries of each chunk,
+    grown until one oracle pass takes about budget_s."""
+    q_lens = np.diff(b.cu_seqlens_q)
+    dec = [int(s) for s in np.nonzero(q_lens == 1)[0]]
+    chunks = [int(s) for s in np.nonzero(q_lens > 1)[0]]
+    order = []
+    for i in range(max(len(dec), len(chunks))):
+        if i < len(chunks):
+            order.append(chunks[i])
+        if i < len(dec):
+            order.append(dec[i])
+    n = 1
+    while True:
+        sb = sub_batch(b, order[:n], chunk_rows=128)
+        t0 = time.perf_counter()
+        oracle_step(sb)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= len(order):
+            return order[:n], sb, dt
+        n = min(len(order), max(n + 1, int(n * min(4.0, budget_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline(b: workloads.Batch, budget_s: float = 15.0):
+    seqs, sb, dt = cpu_sample_plan(b, budget_s / 2)
+    t0 = time.perf_counter()
+    oracle_step(sb)
+    dt = time.perf_counter() - t0
+    toks = int(sb.cu_seqlens_q[-1])
+    return {"value": toks / dt, "unit": "query tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(seqs)} of {b.num_seqs} sequences of the same batch ({toks} query tokens; "
+                      f"chunks cut to their first 128 queries at their own prior context; only "
+                      f"their referenced blocks), append + attention in float64 numpy, {dt:.2f} s"}
+
+
+def run_reference(args, b: workloads.Batch, rank: int, world: int):
+    if rank != 0:
+        return
+    total = args.steps + args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+    seqs, sb, _ = cpu_sample_plan(b, per_step)
+    for _ in range(args.warmup):
+        oracle_step(sb)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sb)
+    dt = time.perf_counter() - t0
+    toks = int(sb.cu_seqlens_q[-1])
+    value = toks * args.steps / dt
+    unit = "query tokens/s"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(b, args),
+        "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": value, "unit": unit,
+                         "sample": f"each step: {len(seqs)} of {b.num_seqs} sequences "
+                                   f"({toks} query tokens; chunks cut to 128 queries)"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(b: workloads.Batch, args):
+    return {"workload": workloads.CONFIGS[WORKLOADS[args.workload]], "seqs": b.num_seqs,
+            "query_tokens": b.num_tokens, "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size, "pages": b.num_pages,
+            "seed": 1000 + WORKLOADS[args.workload],
+            "l2": "flushed before every timed step (512 MiB write); KV also exceeds L2",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    cfg = WORKLOADS[args.workload]
+    b = workloads.make_config(cfg, seed=1000 + cfg + 7919 * rank)
+    if args.impl == "reference":
+        run_reference(args, b, rank, world)
+        return
+
+    import torch
+    import continuous_batching_paged_gb300 as cb
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the CUDA path has no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cb.library()
+
+    def t16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def t32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q, kn, vn = t16(b.q), t16(b.k_new), t16(b.v_new)
+    kp, vp = t16(b.k_pages), t16(b.v_pages)
+    table, cu, kvl = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
+    out = torch.empty_like(q)
+    ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                       b.num_pages, b.max_blocks, b.block_size),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(cb.NUM_PHASE_EVENTS + 1)]
+    for e in ev:
+        e.record()
+
+    def step(record):
+        if record:
+            ev[0].record()
+        cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
+        cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, out=out,
+                                  workspace=ws, decode_ctas=args.decode_ctas,
+                                  phase_events=ev[1:] if record else None)
+
+    # correctness guard before timing: the error word must be clear after one step
+    step(False)
+    cb.check_device_error()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_start = time.perf_counter()
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(False)
+    torch.cuda.synchronize()
+    soak = 0
+    while time.perf_counter() - t_start < 2.0:   # let the clock sampler see the GPU under load
+        flush.fill_(1.0)
+        step(False)
+        soak += 1
+        if soak % 50 == 0:
+            torch.cuda.synchronize()
+
+    names = ["append"] + list(cb.PHASES)
+    acc = {n: 0.0 for n in names}
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    step_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        step(True)
+        ev[-1].synchronize()
+        d = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
+        for n, x in zip(names, d):
+            acc[n] += x
+        step_ms += ev[0].elapsed_time(ev[-1])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    cb.check_device_error()
+
+    ms = dist_max(step_ms / args.steps, world, dev)
+    value = world * b.num_tokens / (ms / 1000.0)
+    per_kernel = {n: acc[n] / args.steps for n in names}
+
+    # e2e: the step through the public API with inputs from pinned host memory, output back.
+    h_q = torch.from_numpy(b.q.view(np.int16)).pin_memory()
+    h_k = torch.from_numpy(b.k_new.view(np.int16)).pin_memory()
+    h_v = torch.from_numpy(b.v_new.view(np.int16)).pin_memory()
+    h_tab = torch.from_numpy(b.block_table).pin_memory()
+    h_cu = torch.from_numpy(b.cu_seqlens_q).pin_memory()
+    h_kv = torch.from_numpy(b.kv_lens).pin_memory()
+    h_out = torch.empty(b.q.shape, dtype=torch.int16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_cu, h_kv))
+    d2h = h_out.numel() * h_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        q.view(torch.int16).copy_(h_q, non_blocking=True)
+        kn.view(torch.int16).copy_(h_k, non_blocking=True)
+        vn.view(torch.int16).copy_(h_v, non_blocking=True)
+        table.copy_(h_tab, non_blocking=True)
+        cu.copy_(h_cu, non_blocking=True)
+        kvl.copy_(h_kv, non_blocking=True)
+        step(False)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        e0.record()
+        e2e_step()
+        e1.record()
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = dist_max(e2e_ms / args.steps, world, dev)
+    cb.check_device_error()
+
+    pk, pk_kind = peaks()
+    dec_bytes, dec_logical = decode_kv_bytes(b)
+    flops = chunk_flops(b)
+    dec_ms, chunk_ms = per_kernel["decode"], per_kernel["chunk"]
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 and dec_bytes else None
+    chunk_tf = flops / (chunk_ms * 1e-3) / 1e12 if chunk_ms > 0 and flops else None
+    if dec_gbs is not None and (chunk_tf is None or dec_ms >= chunk_ms):
+        roof = {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"],
+                "traffic": recorded_traffic("decode_kernel", args.workload),
+                "algorithmic_bytes_per_launch": dec_bytes,
+                "peak_kind": pk_kind, "frac_of_nominal_8000": dec_gbs / NOMINAL_HBM_GBS}
+    else:
+        tpk = pk["bf16_tflops"]
+        roof = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": chunk_tf, "peak": tpk,
+                "unit": "TFLOP/s", "frac": chunk_tf / tpk,
+                "traffic": recorded_traffic("prefill_kernel", args.workload),
+                "algorithmic_flops_per_launch": flops, "peak_kind": pk_kind + " burst bf16"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(b)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(b, args),
+        "e2e": {"value": world * b.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": (1 + 4) * args.steps,
+        "roofline": roof,
+        "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
+                   "gbs": dec_gbs, "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,
+                   "frac_of_nominal_8000": (dec_gbs / NOMINAL_HBM_GBS) if dec_gbs else None},
+        "chunk": {"flops": flops, "tflops": chunk_tf,
+                  "frac_of_burst": (chunk_tf / pk["bf16_tflops"]) if chunk_tf else None,
+                  "frac_of_sustained": (chunk_tf / pk["bf16_tflops_sustained"]) if chunk_tf else None},
+        "kernel_ms": per_kernel,
+        "clocks": sampler.summary(),
+        "cpu_baseline": cpu,
+        "wall_s_timed": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,306 @@
+// C ABI of libcb (see include/cb.h): host-side validation, TMA descriptor encoding, launches,
+// and the per-device error word.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "cb_common.cuh"
+#include "cb_launch.h"
+
+namespace {
+
+__device__ uint32_t g_cb_error_word;
+
+thread_local std::string t_last_error;
+
+cb_status fail(cb_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+cb_status fail(cb_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+cb_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  uint32_t* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cb_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(CB_ERR_UNSUPPORTED, "device id %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(CB_ERR_UNSUPPORTED, "libcb is built for sm_103a; device %d is sm_%d%d", dev,
+                  major, minor);
+    e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_cb_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    st.err = static_cast<uint32_t*>(p);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return CB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int gcd_int(int x, int y) {
+  while (y) {
+    const int t = x % y;
+    x = y;
+    y = t;
+  }
+  return x;
+}
+
+cb_status check_dims(const cb_dims* d, int32_t block_size) {
+  if (d == nullptr) return fail(CB_ERR_INVALID_ARG, "dims is NULL");
+  if (block_size < 4)
+    return fail(CB_ERR_INVALID_ARG, "block_size must be at least 4, got %d", block_size);
+  if (d->num_seqs < 0 || d->num_tokens < 0)
+    return fail(CB_ERR_INVALID_ARG, "negative num_seqs or num_tokens");
+  if (d->num_q_heads < 1 || d->num_kv_heads < 1)
+    return fail(CB_ERR_INVALID_ARG, "num_q_heads and num_kv_heads must be >= 1");
+  if (d->num_q_heads % d->num_kv_heads != 0)
+    return fail(CB_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                d->num_q_heads, d->num_kv_heads);
+  if (d->num_pages < 1 || d->max_blocks_per_seq < 1)
+    return fail(CB_ERR_INVALID_ARG, "num_pages and max_blocks_per_seq must be >= 1");
+  if ((long long)d->num_pages * block_size >= (1LL << 31))
+    return fail(CB_ERR_INVALID_ARG, "num_pages * block_size must be < 2^31");
+  if ((long long)d->max_blocks_per_seq * block_size >= (1LL << 31))
+    return fail(CB_ERR_INVALID_ARG, "max_blocks_per_seq * block_size must be < 2^31");
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(CB_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", d->head_dim);
+  return CB_OK;
+}
+
+cb_status encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t box_rows) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  const cuuint32_t box[3] = {64, 1, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return CB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t cb_version(void) { return 100; }
+
+const char* cb_status_string(cb_status s) {
+  switch (s) {
+    case CB_OK: return "CB_OK";
+    case CB_ERR_INVALID_ARG: return "CB_ERR_INVALID_ARG";
+    case CB_ERR_UNSUPPORTED: return "CB_ERR_UNSUPPORTED";
+    case CB_ERR_OUT_OF_RANGE: return "CB_ERR_OUT_OF_RANGE";
+    case CB_ERR_TIMEOUT: return "CB_ERR_TIMEOUT";
+    case CB_ERR_CUDA: return "CB_ERR_CUDA";
+  }
+  return "CB_ERR_UNKNOWN";
+}
+
+const char* cb_last_error_message(void) { return t_last_error.c_str(); }
+
+size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size) {
+  if (check_dims(dims, block_size) != CB_OK) return 0;
+  return cb::ws_layout(dims->num_seqs, dims->num_q_heads, dims->head_dim).total;
+}
+
+cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                       const int32_t* kv_lens, int32_t block_size, const cb_dims* dims,
+                       void* stream) {
+  t_last_error.clear();
+  cb_status st = check_dims(dims, block_size);
+  if (st != CB_OK) return st;
+  if (dims->num_tokens == 0) return CB_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !cu_seqlens_q || !kv_lens)
+    return fail(CB_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return fail(CB_ERR_INVALID_ARG, "K/V tensors must be 16-byte aligned");
+  if (dims->num_seqs == 0) return fail(CB_ERR_INVALID_ARG, "tokens without sequences");
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != CB_OK) return st;
+  cb::AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.block_table = block_table;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.kv_lens = kv_lens;
+  a.S = dims->num_seqs;
+  a.T = dims->num_tokens;
+  a.Hkv = dims->num_kv_heads;
+  a.D = dims->head_dim;
+  a.bs = block_size;
+  a.max_blocks = dims->max_blocks_per_seq;
+  a.P = dims->num_pages;
+  a.err = ds->err;
+  cudaError_t e = cb::launch_kv_append(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return CB_OK;
+}
+
+cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                       const int32_t* kv_lens, int32_t block_size, float scale,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, const cb_dims* dims,
+                                       const cb_options* options, void* stream) {
+  t_last_error.clear();
+  cb_status st = check_dims(dims, block_size);
+  if (st != CB_OK) return st;
+  if (dims->num_tokens == 0) return CB_OK;
+  if (dims->num_seqs == 0) return fail(CB_ERR_INVALID_ARG, "tokens without sequences");
+  if (!q || !k_pages || !v_pages || !block_table || !cu_seqlens_q || !kv_lens || !out || !workspace)
+    return fail(CB_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return fail(CB_ERR_INVALID_ARG, "q, pages and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(CB_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(CB_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!(scale > 0.f) || scale != scale)
+    return fail(CB_ERR_INVALID_ARG, "scale must be a positive finite number");
+  const size_t need = cb::ws_layout(dims->num_seqs, dims->num_q_heads, dims->head_dim).total;
+  if (workspace_bytes < need)
+    return fail(CB_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  const int Hq = dims->num_q_heads, Hkv = dims->num_kv_heads, G = Hq / Hkv;
+  if (G > 16) return fail(CB_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
+  if (Hkv > cb::kMaxDecodeHeadsPerCta && Hkv % cb::kMaxDecodeHeadsPerCta != 0)
+    return fail(CB_ERR_UNSUPPORTED, "num_kv_heads > 8 must be a multiple of 8");
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != CB_OK) return st;
+
+  cb::AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.lse = lse;
+  a.block_table = block_table;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.kv_lens = kv_lens;
+  a.ws = static_cast<char*>(workspace);
+  a.err = ds->err;
+  a.S = dims->num_seqs;
+  a.T = dims->num_tokens;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.D = dims->head_dim;
+  a.bs = block_size;
+  a.max_blocks = dims->max_blocks_per_seq;
+  a.P = dims->num_pages;
+  a.KB = gcd_int(block_size, 16);
+  int dctas = options != nullptr ? options->decode_ctas : 0;
+  if (dctas <= 0) dctas = ds->sm_count;
+  if (dctas > CB_MAX_DECODE_CTAS) dctas = CB_MAX_DECODE_CTAS;
+  a.decode_ctas = dctas;
+  a.prefill_ctas = ds->sm_count;
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  CUtensorMap qmap, kmap, vmap;
+  const uint64_t D = (uint64_t)a.D;
+  const uint64_t rows = (uint64_t)a.P * (uint64_t)block_size;
+  if ((st = encode_map(&kmap, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
+  if ((st = encode_map(&vmap, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
+  if ((st = encode_map(&qmap, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 128)) != CB_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* const* ev = options != nullptr ? options->phase_events : nullptr;
+  auto mark = [&](int i) -> cudaError_t {
+    return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess && (e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess && (e = cb::launch_decode(a, kmap, vmap, s)) != cudaSuccess)
+    return cuda_fail(e, "decode launch");
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess && (e = cb::launch_merge(a, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
+  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess && (e = cb::launch_prefill(a, qmap, kmap, vmap, s)) != cudaSuccess)
+    return cuda_fail(e, "prefill launch");
+  if (e == cudaSuccess) e = mark(4);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  return CB_OK;
+}
+
+cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const void* v_pages,
+                                    const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                    const int32_t* kv_lens, int32_t block_size, float scale,
+                                    void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, const cb_dims* dims, void* stream) {
+  return cb_ragged_paged_attention_ex(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
+                                      block_size, scale, out, lse, workspace, workspace_bytes,
+                                      dims, nullptr, stream);
+}
+
+cb_status cb_get_device_error(void* stream) {
+  t_last_error.clear();
+  DeviceState* ds = nullptr;
+  cb_status st = device_state(&ds);
+  if (st != CB_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t bits = 0;
+  e = cudaMemcpy(&bits, ds->err, sizeof(bits), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (bits != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  if (bits & cb::kErrTimeout) return fail(CB_ERR_TIMEOUT, "a device-side wait expired");
+  if (bits & cb::kErrOutOfRange)
+    return fail(CB_ERR_OUT_OF_RANGE, "device saw metadata outside the pool, table or lengths");
+  return CB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,187 @@
+// Paged KV-append: scatter this step's K/V rows into their cache slots, and the batch planner
+// of the attention pass.
+//
+// Slot rule ("LLM learning path 3.3 Batching & Memory Management", section "PagedAttention:
+// block tables"): token position p of a sequence lives in physical block table[p / bs] at
+// offset p % bs; with the token-major pool of "Continuous batching in transformers"
+// (paged-cache section) that is row table[p / bs] * bs + p % bs of the flattened
+// [P * bs, Hkv, D] tensor.  Token i of sequence s has position kv_len_s - q_len_s + i.
+#include "cb_common.cuh"
+#include "cb_launch.h"
+
+namespace cb {
+
+// One thread copies one 16-byte chunk of K and the same chunk of V.
+__global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
+  const int cpr = a.D / 8;                       // 16-byte chunks per (token, head) row
+  const long long per_tok = (long long)a.Hkv * cpr;
+  const long long total = (long long)a.T * per_tok;
+  const uint4* kn = static_cast<const uint4*>(a.k_new);
+  const uint4* vn = static_cast<const uint4*>(a.v_new);
+  uint4* kp = static_cast<uint4*>(a.k_pages);
+  uint4* vp = static_cast<uint4*>(a.v_pages);
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / per_tok);
+    const int rem = (int)(idx - (long long)t * per_tok);
+    // Sequence of token t: the last s with cu[s] <= t (cu is non-decreasing).
+    int lo = 0, hi = a.S;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    if (s >= a.S) { report(a.err, kErrOutOfRange); continue; }
+    const int c0 = __ldg(a.cu_seqlens_q + s), c1 = __ldg(a.cu_seqlens_q + s + 1);
+    const int q_len = c1 - c0;
+    const int kv = __ldg(a.kv_lens + s);
+    if (t < c0 || t >= c1 || kv < q_len) { report(a.err, kErrOutOfRange); continue; }
+    const int pos = kv - q_len + (t - c0);
+    const int lb = pos / a.bs;
+    if (lb >= a.max_blocks) { report(a.err, kErrOutOfRange); continue; }
+    const int blk = __ldg(a.block_table + (size_t)s * a.max_blocks + lb);
+    if (blk < 0 || blk >= a.P) { report(a.err, kErrOutOfRange); continue; }
+    const long long slot = (long long)blk * a.bs + (pos - lb * a.bs);
+    const long long dst = slot * per_tok + rem;
+    kp[dst] = __ldg(kn + idx);
+    vp[dst] = __ldg(vn + idx);
+  }
+}
+
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
+  const long long total = (long long)a.T * a.Hkv * (a.D / 8);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Planner: one CTA classifies every sequence (q_len == 1 -> decode, q_len > 1 -> chunk),
+// validates its lengths, and writes the compacted lists and prefix sums the attention passes
+// read.  Nothing returns to the host.
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive block-wide scan of four counters at once; returns the block totals in tot[].
+__device__ __forceinline__ void block_scan4(int v[4], int ex[4], int tot[4], int (*sw)[4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int x = v[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    inc[k] = x;
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sw[warp][k] = inc[k];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int x = sw[lane][k];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      sw[lane][k] = x;  // inclusive over warps
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ex[k] = inc[k] - v[k] + (warp > 0 ? sw[warp - 1][k] : 0);
+    tot[k] = sw[31][k];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
+  __shared__ int sw[32][4];
+  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
+  int32_t* dec_seq = reinterpret_cast<int32_t*>(a.ws + L.dec_seq);
+  int32_t* dec_prefix = reinterpret_cast<int32_t*>(a.ws + L.dec_prefix);
+  int32_t* cta_first = reinterpret_cast<int32_t*>(a.ws + L.cta_first);
+  int32_t* pf_seq = reinterpret_cast<int32_t*>(a.ws + L.pf_seq);
+  int32_t* pf_prefix = reinterpret_cast<int32_t*>(a.ws + L.pf_prefix);
+  const int tid = threadIdx.x;
+  const long long max_kv = (long long)a.max_blocks * a.bs;
+
+  if (tid == 0) {
+    if (a.cu_seqlens_q[0] != 0 || a.cu_seqlens_q[a.S] != a.T) report(a.err, kErrOutOfRange);
+  }
+  int carry[4] = {0, 0, 0, 0};
+  for (int base = 0; base < a.S; base += kPlanThreads) {
+    const int s = base + tid;
+    int v[4] = {0, 0, 0, 0};
+    if (s < a.S) {
+      const int c0 = a.cu_seqlens_q[s], c1 = a.cu_seqlens_q[s + 1];
+      const int q_len = c1 - c0;
+      const int kv = a.kv_lens[s];
+      const bool ok = c0 >= 0 && c1 <= a.T && q_len >= 0 && kv >= q_len && kv <= max_kv;
+      if (!ok) {
+        report(a.err, kErrOutOfRange);
+      } else if (q_len == 1) {
+        v[0] = 1;
+        v[1] = (kv + kDecodeTileKeys - 1) / kDecodeTileKeys;
+      } else if (q_len > 1) {
+        v[2] = 1;
+        v[3] = (q_len + kPrefillTileM - 1) / kPrefillTileM;
+      }
+    }
+    int ex[4], tot[4];
+    block_scan4(v, ex, tot, sw);
+    if (v[0]) {
+      dec_seq[carry[0] + ex[0]] = s;
+      dec_prefix[carry[0] + ex[0]] = carry[1] + ex[1];
+    }
+    if (v[2]) {
+      pf_seq[carry[2] + ex[2]] = s;
+      pf_prefix[carry[2] + ex[2]] = carry[3] + ex[3];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) carry[k] += tot[k];
+  }
+  if (tid == 0) {
+    dec_prefix[carry[0]] = carry[1];
+    pf_prefix[carry[2]] = carry[3];
+    hdr->n_dec = carry[0];
+    hdr->dec_tiles = carry[1];
+    hdr->n_pf = carry[2];
+    hdr->pf_qtiles = carry[3];
+    hdr->pf_counter = 0;
+  }
+  __syncthreads();
+  // First decode sequence of each decode CTA: CTA c owns tiles [c*n/N, (c+1)*n/N), with N
+  // capped at the tile count so that no CTA range is empty.
+  const int n_dec = carry[0];
+  const long long ntiles = carry[1];
+  const int N = (int)(ntiles < a.decode_ctas ? (ntiles > 0 ? ntiles : 1) : a.decode_ctas);
+  if (tid == 0) hdr->decode_ctas = N;
+  for (int c = tid; c <= N; c += kPlanThreads) {
+    const long long t0 = ntiles * c / N;
+    int lo = 0, hi = n_dec;  // largest d in [0, n_dec] with dec_prefix[d] <= t0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (dec_prefix[mid] <= t0) lo = mid; else hi = mid - 1;
+    }
+    cta_first[c] = lo;
+  }
+}
+
+cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cb

@@ -1,0 +1,445 @@
+// Decode pass of ragged paged attention: every sequence with q_len == 1 attends to all of its
+// kv_len keys.  "Decode still reads the full KV every step" ("LLM learning path 3.3 Batching &
+// Memory Management", section "Common pitfalls"), so this pass is bound by HBM bandwidth and
+// is built around moving K/V pages at full rate:
+//
+//   * The key tiles of all decode sequences are laid end to end (16 keys per tile) and cut into
+//     `decode_ctas` equal contiguous ranges, one per CTA: every CTA streams the same number of
+//     bytes whatever the length mix.  A sequence cut by a range boundary is finished by the
+//     merge kernel from per-CTA partial results (m, l, o): the split-KV scheme with an online
+//     softmax and a log-sum-exp merge.
+//   * One producer warp walks the range, prefetches block-table entries 32 at a time, and
+//     issues TMA tensor copies (128-byte swizzle) of each (page run, KV head, 64-wide half of D)
+//     into a multi-stage shared-memory ring guarded by mbarriers.
+//   * One consumer warp per KV head computes S = Q K^T and O += P V for the G query heads of its
+//     group with mma.sync m16n8k16 (bf16 in, fp32 accumulate); the G rows of a GQA group share
+//     every K/V byte read from HBM.  Softmax state lives in registers; row maxima and sums are
+//     reduced with warp shuffles.
+//
+// Online softmax: for each new tile, m' = max(m, max_j x_j), rescale (l, o) by 2^(m - m'),
+// then add 2^(x_j - m') and 2^(x_j - m') v_j; x_j = scale * log2(e) * q.k_j.
+#include "cb_common.cuh"
+#include "cb_launch.h"
+
+namespace cb {
+
+constexpr int kDecodeStages = 3;
+constexpr uint32_t kInfoFirst = 1u, kInfoLast = 2u, kInfoComplete = 4u;
+
+struct StageInfo {
+  int seq;       // sequence id
+  int dec;       // index among decode sequences (partial-result slot = cta + dec)
+  int tok;       // packed token index of the sequence's query
+  int kv;        // kv_len
+  int key0;      // first key of this tile
+  uint32_t flags;
+  int pad[2];
+};
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kHalfBytes = kMaxDecodeHeadsPerCta * kDecodeTileKeys * 128;  // 16 KB
+  static constexpr int kKVBytes = kHalves * kHalfBytes;                             // K or V
+  static constexpr int kStageBytes = 2 * kKVBytes;
+  static constexpr int kBarOffset = kDecodeStages * kStageBytes;
+  static constexpr int kInfoOffset = kBarOffset + 2 * kDecodeStages * 8;
+  static constexpr int kTotal = kInfoOffset + kDecodeStages * (int)sizeof(StageInfo) + 1024;
+};
+
+// Largest CTA index c in [0, N) whose range start floor(c * n / N) is <= t.
+__device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (n * mid / N <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
+    decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+  using SM = DecodeSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + SM::kBarOffset;              // kDecodeStages x 8 B
+  const uint32_t bar_empty = bar_full + kDecodeStages * 8;       // kDecodeStages x 8 B
+  StageInfo* info = reinterpret_cast<StageInfo*>(smem + SM::kInfoOffset);
+
+  const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x, hg = blockIdx.y;
+  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
+  const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
+  const int32_t* dec_prefix = reinterpret_cast<const int32_t*>(a.ws + L.dec_prefix);
+  const int32_t* cta_first = reinterpret_cast<const int32_t*>(a.ws + L.cta_first);
+
+  const long long ntiles = hdr->dec_tiles;
+  const int N = hdr->decode_ctas;  // planner's CTA count: <= gridDim.x, every range non-empty
+  if (c >= N) return;
+  const long long t0 = ntiles * c / N, t1 = ntiles * (c + 1) / N;
+  if (t0 >= t1) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecodeStages; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, HB);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == HB) {
+    // ===================================================================== producer warp
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+    const int KB = a.KB;
+    const int nsb = kDecodeTileKeys / KB;        // TMA boxes per head per tile
+    const int tiles_per_batch = 32 / nsb;
+    int d = cta_first[c];
+    long long t = t0;
+    long long it = 0;
+    bool abort = false;
+    while (t < t1 && !abort) {
+      if (d >= hdr->n_dec) { report(a.err, kErrOutOfRange); break; }
+      const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
+      const int s = dec_seq[d];
+      const int kv = a.kv_lens[s];
+      const int tok = a.cu_seqlens_q[s];
+      const long long lo = t > p0 ? t : p0;
+      const long long hi = t1 < p1 ? t1 : p1;
+      const bool complete = p0 >= t0 && p1 <= t1;
+      const int32_t* row = a.block_table + (size_t)s * a.max_blocks;
+      for (long long tb = lo; tb < hi && !abort; tb += tiles_per_batch) {
+        // Prefetch the block-table entries of up to 32 (tile, sub-box) pairs.
+        int entry = -1;
+        {
+          const long long tile = tb + lane / nsb;
+          const int pos = (int)(tile - p0) * kDecodeTileKeys + (lane % nsb) * KB;
+          if (lane < tiles_per_batch * nsb && tile < hi && pos < kv) {
+            const int lb = pos / a.bs;
+            entry = lb < a.max_blocks ? __ldg(row + lb) : -2;
+          }
+        }
+        const int nb = (int)((hi - tb) < tiles_per_batch ? (hi - tb) : tiles_per_batch);
+        for (int tl = 0; tl < nb; ++tl, ++it) {
+          const long long tile = tb + tl;
+          const int stage = (int)(it % kDecodeStages);
+          const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+          if (lane == 0 && !mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
+            report(a.err, kErrTimeout);
+            abort = true;
+          }
+          abort = __shfl_sync(0xffffffffu, abort, 0);
+          if (abort) break;
+          const int key0 = (int)(tile - p0) * kDecodeTileKeys;
+          // (sub-box sb, head h) pairs of this tile, 32 per pass over the warp.
+          const int npairs = nsb * HB;
+          uint32_t nvalid = 0;
+          for (int base = 0; base < npairs; base += 32) {
+            const int pr = base + lane, sb = pr / HB;
+            const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (sb < nsb ? sb : 0));
+            const int pos = key0 + sb * KB;
+            const bool want = pr < npairs && pos < kv;
+            const bool valid = want && e >= 0 && e < a.P;
+            if (want && !valid) report(a.err, kErrOutOfRange);
+            nvalid += __popc(__ballot_sync(0xffffffffu, valid));
+          }
+          if (lane == 0) {
+            StageInfo& si = info[stage];
+            si.seq = s;
+            si.dec = d;
+            si.tok = tok;
+            si.kv = kv;
+            si.key0 = key0;
+            si.flags = (tile == lo ? kInfoFirst : 0u) | (tile == hi - 1 ? kInfoLast : 0u) |
+                       (complete ? kInfoComplete : 0u);
+            mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                  nvalid * (uint32_t)(2 * SM::kHalves * KB * 128));
+          }
+          __syncwarp();
+          for (int base = 0; base < npairs; base += 32) {
+            const int pr = base + lane, sb = pr / HB, h = pr % HB;
+            const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (sb < nsb ? sb : 0));
+            const int pos = key0 + sb * KB;
+            const bool valid = pr < npairs && pos < kv && e >= 0 && e < a.P;
+            if (valid) {
+              const int token = e * a.bs + (pos % a.bs);
+              const int head = hg * kMaxDecodeHeadsPerCta + h;
+              const uint32_t kst = sbase + stage * SM::kStageBytes;
+              const uint32_t vst = kst + SM::kKVBytes;
+              const uint32_t off = (uint32_t)(h * kDecodeTileKeys * 128 + sb * KB * 128);
+#pragma unroll
+              for (int half = 0; half < SM::kHalves; ++half) {
+                tma_load_3d(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
+                            half * 64, head, token);
+                tma_load_3d(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
+                            half * 64, head, token);
+              }
+            }
+          }
+        }
+      }
+      t = hi;
+      ++d;
+    }
+  } else if (warp < HB) {
+    // ===================================================================== consumer warps
+    const int h = warp;                                    // KV head within this CTA
+    const int kvh = hg * kMaxDecodeHeadsPerCta + h;        // global KV head
+    const int g = lane >> 2, tq = lane & 3;                // mma fragment coordinates
+    const float2* dummy = nullptr;
+    (void)dummy;
+    float2* part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml);
+    float* part_o = reinterpret_cast<float*>(a.ws + L.part_o);
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+    __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
+
+    constexpr int KS = D / 16;   // k-steps over the head dimension
+    constexpr int NT = D / 8;    // n-tiles of the output
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const long long n_my = t1 - t0;
+    for (long long it = 0; it < n_my; ++it) {
+      const int stage = (int)(it % kDecodeStages);
+      const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+      if (!mbar_wait(bar_full + 8 * stage, phase)) {
+        report(a.err, kErrTimeout);
+        break;
+      }
+      const StageInfo si = info[stage];
+      if (si.flags & kInfoFirst) {
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        // Query fragments (rows = the G query heads of this KV head; rows >= G are zero).
+        const int r0 = g, r1 = g + 8;
+        const bool v0 = r0 < a.G, v1 = r1 < a.G;
+        const uint32_t* q0 =
+            reinterpret_cast<const uint32_t*>(qg + ((size_t)si.tok * a.Hq + kvh * a.G + r0) * D);
+        const uint32_t* q1 =
+            reinterpret_cast<const uint32_t*>(qg + ((size_t)si.tok * a.Hq + kvh * a.G + r1) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int w = (ks * 16 + 2 * tq) / 2;
+          qa[ks][0] = v0 ? __ldg(q0 + w) : 0u;
+          qa[ks][1] = v1 ? __ldg(q1 + w) : 0u;
+          qa[ks][2] = v0 ? __ldg(q0 + w + 4) : 0u;
+          qa[ks][3] = v1 ? __ldg(q1 + w + 4) : 0u;
+        }
+      }
+      const uint32_t kst = sbase + stage * SM::kStageBytes;
+      const uint32_t vst = kst + SM::kKVBytes;
+      const int rowbase = h * kDecodeTileKeys;
+
+      // ---- S = Q K^T over this tile's 16 keys (two n-tiles of 8 keys)
+      float s[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+      {
+        const int kk = (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int half = ks >> 2;
+          const int chunk = ((ks & 3) << 1) + csel;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sw128(kst + half * SM::kHalfBytes, rowbase + kk, chunk), b0, b1, b2, b3);
+          mma_bf16_16816(s[0], qa[ks], b0, b1);
+          mma_bf16_16816(s[1], qa[ks], b2, b3);
+        }
+      }
+      const bool tail = si.key0 + kDecodeTileKeys > si.kv;
+      if (tail) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int key = si.key0 + nt * 8 + 2 * tq + (j & 1);
+            if (key >= si.kv) s[nt][j] = -INFINITY;
+          }
+      }
+      // ---- online softmax (rows g and g + 8)
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])) * a.scale_log2;
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])) * a.scale_log2;
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = fast_exp2(fmaf(s[nt][0], a.scale_log2, -mn0));
+        p[nt][1] = fast_exp2(fmaf(s[nt][1], a.scale_log2, -mn0));
+        p[nt][2] = fast_exp2(fmaf(s[nt][2], a.scale_log2, -mn1));
+        p[nt][3] = fast_exp2(fmaf(s[nt][3], a.scale_log2, -mn1));
+      }
+      l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+      l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= al0;
+        o[nt][1] *= al0;
+        o[nt][2] *= al1;
+        o[nt][3] *= al1;
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+
+      // ---- keys past kv_len: their V rows may hold stale or poison data; P is 0 there, but
+      // 0 * NaN is NaN, so zero those rows of this head before they enter the product.
+      if (tail) {
+        const int first = si.kv - si.key0;  // 1..15
+        const int nrow = kDecodeTileKeys - first;
+        for (int i = lane; i < nrow * SM::kHalves * 8; i += 32) {
+          const int r = first + i / (SM::kHalves * 8);
+          const int rem = i % (SM::kHalves * 8);
+          const int half = rem >> 3, ch = rem & 7;
+          const uint32_t addr = sw128(vst + half * SM::kHalfBytes, rowbase + r, ch);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+        __syncwarp();
+      }
+      // ---- O += P V
+      {
+        const int kk = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+          const int cidx = 2 * np + csel;
+          const int half = cidx >> 3;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sw128(vst + half * SM::kHalfBytes, rowbase + kk, cidx & 7), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * np], pa, b0, b1);
+          mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+        }
+      }
+      if (tail) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+
+      if (si.flags & kInfoLast) {
+        float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+        float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+        const int rows[2] = {g, g + 8};
+        const float ls[2] = {lt0, lt1};
+        const float ms[2] = {m0, m1};
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          if (rows[hr] >= a.G) continue;
+          const int head = kvh * a.G + rows[hr];
+          if (si.flags & kInfoComplete) {
+            const float inv = 1.f / ls[hr];
+            uint32_t* dst =
+                reinterpret_cast<uint32_t*>(outg + ((size_t)si.tok * a.Hq + head) * D);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              dst[(nt * 8 + 2 * tq) / 2] =
+                  pack_bf16x2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
+            if (a.lse != nullptr && tq == 0)
+              a.lse[(size_t)si.tok * a.Hq + head] = (ms[hr] + __log2f(ls[hr])) * 0.6931471805599453f;
+          } else {
+            const size_t slot = (size_t)c + si.dec;
+            float* po = part_o + (slot * a.Hq + head) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              *reinterpret_cast<float2*>(po + nt * 8 + 2 * tq) =
+                  make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
+            if (tq == 0) part_ml[slot * a.Hq + head] = make_float2(ms[hr], ls[hr]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Combine the partial (m, l, o) of decode sequences whose tiles span several CTAs.
+__global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a) {
+  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
+  const int d = blockIdx.x;
+  if (d >= hdr->n_dec) return;
+  const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
+  const int32_t* dec_prefix = reinterpret_cast<const int32_t*>(a.ws + L.dec_prefix);
+  const float2* part_ml = reinterpret_cast<const float2*>(a.ws + L.part_ml);
+  const float* part_o = reinterpret_cast<const float*>(a.ws + L.part_o);
+  const long long n = hdr->dec_tiles;
+  const int N = hdr->decode_ctas;
+  const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
+  const int cf = cta_of_tile(p0, n, N), cl = cta_of_tile(p1 - 1, n, N);
+  if (cf == cl) return;  // written directly by the decode pass
+  const int s = dec_seq[d];
+  const int tok = a.cu_seqlens_q[s];
+  __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
+  for (int idx = threadIdx.x; idx < a.Hq * a.D; idx += blockDim.x) {
+    const int head = idx / a.D, dd = idx % a.D;
+    float M = -INFINITY;
+    for (int cc = cf; cc <= cl; ++cc) {
+      if (n * cc / N == n * (cc + 1) / N) continue;  // empty range: wrote no partial
+      M = fmaxf(M, part_ml[((size_t)cc + d) * a.Hq + head].x);
+    }
+    float Lsum = 0.f, O = 0.f;
+    for (int cc = cf; cc <= cl; ++cc) {
+      if (n * cc / N == n * (cc + 1) / N) continue;
+      const size_t slot = (size_t)cc + d;
+      const float2 ml = part_ml[slot * a.Hq + head];
+      const float w = fast_exp2(ml.x - M);
+      Lsum += ml.y * w;
+      O += part_o[(slot * a.Hq + head) * a.D + dd] * w;
+    }
+    outg[((size_t)tok * a.Hq + head) * a.D + dd] = __float2bfloat16_rn(O / Lsum);
+    if (dd == 0 && a.lse != nullptr)
+      a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
+  }
+}
+
+template <int D>
+static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, cudaStream_t stream) {
+  using SM = DecodeSmem<D>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
+  dim3 grid(a.decode_ctas, (a.Hkv + kMaxDecodeHeadsPerCta - 1) / kMaxDecodeHeadsPerCta);
+  decode_kernel<D><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+  if (a.D == 128) return launch_decode_d<128>(a, kmap, vmap, stream);
+  return launch_decode_d<64>(a, kmap, vmap, stream);
+}
+
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
+  if (a.S == 0) return cudaSuccess;
+  merge_kernel<<<a.S, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cb

@@ -1,0 +1,46 @@
+// Internal launch interface between the C ABI (cb_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cb {
+
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_pages;
+  void* v_pages;
+  const int32_t* block_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  int S, T, Hkv, D, bs, max_blocks, P;
+  uint32_t* err;
+};
+
+struct AttnArgs {
+  const void* q;
+  void* out;
+  float* lse;
+  const int32_t* block_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  char* ws;
+  uint32_t* err;
+  int S, T, Hq, Hkv, G, D, bs, max_blocks, P;
+  int KB;              // rows per TMA box on the page pool: gcd(bs, 16)
+  int decode_ctas;     // CTAs of the decode pass (<= CB_MAX_DECODE_CTAS)
+  int prefill_ctas;    // persistent CTAs of the prefill pass
+  float scale_log2;    // softmax scale * log2(e)
+};
+
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream);
+
+}  // namespace cb

@@ -1,0 +1,166 @@
+/*
+ * cb.h -- C ABI of libcb: paged KV-append and ragged paged attention on one GB300 (sm_103a).
+ *
+ * The problem these calls solve is the attention step of a continuous-batching engine:
+ * every token of one forward pass (decode tokens and chunked-prefill chunks alike) is packed
+ * into a single ragged token axis delimited by cu_seqlens_q, and each sequence's keys and
+ * values live in fixed-size blocks of a paged KV cache reached through a per-sequence block
+ * table ("LLM learning path 3.3 Batching & Memory Management", sections "Continuous
+ * (iteration-level) batching", "PagedAttention: block tables" and "Chunked prefill";
+ * "Continuous batching in transformers", section "The paged cache, its two reserved blocks,
+ * and the block-size trade"; continuous-batching architecture doc, section "Memory
+ * management").
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is DEVICE memory owned by the caller, C-contiguous, and must stay
+ *     valid until the work queued on `stream` has finished.  The library allocates nothing per
+ *     call; its only device state is one 32-bit error word per device.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *     calls are asynchronous on that stream unless stated otherwise.
+ *   - bf16 tensors are passed as void*; 16-byte alignment is required for every tensor.
+ *   - Host-side checks (null pointers, sizes, alignment, unsupported shapes) are made before
+ *     anything is queued; a failing check returns an error and queues nothing.
+ *     cb_last_error_message() then describes it.
+ *   - Device-side checks (metadata that only the GPU reads: block ids, lengths) never trap:
+ *     the kernel skips the offending access, its outputs for that sequence are unspecified,
+ *     and it records the fault in the device error word; cb_get_device_error() reports it.
+ *
+ * Shapes (S sequences, T packed tokens, Hq query heads, Hkv KV heads, D head dim,
+ *         P pages-blocks in the pool, bs block size, MB max blocks per sequence)
+ *   q, out            bf16  [T, Hq, D]
+ *   k_new, v_new      bf16  [T, Hkv, D]
+ *   k_pages, v_pages  bf16  [P, bs, Hkv, D]   token-major: row (block*bs + offset) of the
+ *                                             flattened [P*bs, Hkv, D] tensor is one token
+ *   block_table       int32 [S, MB]           entry j = physical block holding tokens
+ *                                             [j*bs, (j+1)*bs) of the sequence; unused
+ *                                             entries are never read
+ *   cu_seqlens_q      int32 [S+1]             cu[0] = 0, non-decreasing, cu[S] = T
+ *   kv_lens           int32 [S]               keys visible to sequence s INCLUDING this
+ *                                             step's appended tokens (kv_len >= q_len)
+ *   lse               fp32  [T, Hq]           optional natural-log softmax normaliser
+ * Query token i of sequence s sits at absolute position ctx_s + i, ctx_s = kv_len_s - q_len_s,
+ * and attends to keys 0 .. ctx_s + i of its own sequence (causal mask offset by the prior
+ * context); query head h reads KV head h / (Hq / Hkv).
+ */
+#ifndef CB_H_
+#define CB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned tensor, block_size < 4 */
+  CB_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement (e.g. D) */
+  CB_ERR_OUT_OF_RANGE = 3,  /* device saw metadata outside the pool / table / lengths     */
+  CB_ERR_TIMEOUT = 4,       /* a device-side wait gave up (bounded waits, no hang)        */
+  CB_ERR_CUDA = 5           /* a CUDA runtime or driver call failed                       */
+} cb_status;
+
+typedef struct {
+  int32_t num_seqs;            /* S  >= 0                                           */
+  int32_t num_tokens;          /* T  >= 0, must equal cu_seqlens_q[S]               */
+  int32_t num_q_heads;         /* Hq >= 1, a multiple of Hkv, Hq / Hkv <= 16        */
+  int32_t num_kv_heads;        /* Hkv >= 1                                          */
+  int32_t head_dim;            /* D: 64 or 128                                      */
+  int32_t num_pages;           /* P  >= 1 blocks in the pool (P * bs < 2^31)        */
+  int32_t max_blocks_per_seq;  /* MB >= 1 columns of block_table                    */
+} cb_dims;
+
+/*
+ * cb_kv_append -- scatter this step's K/V rows into their cache slots.
+ *
+ * Token i of sequence s (packed row cu[s] + i) has position pos = ctx_s + i and is copied,
+ * bit for bit, to flattened page row block_table[s][pos / bs] * bs + pos % bs, for K and for V
+ * ("LLM learning path 3.3", section "PagedAttention: block tables": token position p lives
+ * in block table[p // bs] at offset p % bs; architecture doc, section "Memory management":
+ * the kernels write the blocks a request's table names).  Only those T*Hkv*D elements of
+ * each pool are written.
+ * Undefined when two tokens map to the same slot or when a written block is shared with
+ * another sequence's visible keys (copy-on-write is the block manager's job).
+ * Device errors (CB_ERR_OUT_OF_RANGE via cb_get_device_error): kv_len < q_len,
+ * pos / bs >= MB, block id outside [0, P), malformed cu_seqlens_q.  The row is skipped.
+ */
+cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                       const int32_t* kv_lens, int32_t block_size, const cb_dims* dims,
+                       void* stream);
+
+/*
+ * cb_attention_workspace_size -- bytes of device scratch cb_ragged_paged_attention needs.
+ * Pure host arithmetic on (dims, block_size); 0 when dims is NULL or invalid.  The
+ * workspace holds the batch plan and the fp32 partial results of split decode sequences.
+ */
+size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size);
+
+/*
+ * cb_ragged_paged_attention -- one attention forward pass over the ragged batch.
+ *
+ * out[t, h, :] = sum_j softmax_j(scale * q[t,h,:] . K_s[j,g,:]) * V_s[j,g,:] over the keys
+ * j <= ctx_s + i of t's own sequence s, with K_s/V_s gathered through block_table and
+ * g = h / (Hq/Hkv).  Inputs are bf16, accumulation is fp32, out is rounded to bf16.
+ * If lse is not NULL it receives the natural log of each row's softmax normaliser.
+ * Sequences with q_len == 0 are skipped; the pass reads the pages after cb_kv_append wrote
+ * them (kv_lens include the appended tokens).  out must not alias q or the pages.
+ * workspace: device memory of at least cb_attention_workspace_size(dims, block_size) bytes,
+ * 256-byte aligned, owned by the caller and not used by other work while this call runs.
+ * Device errors as for cb_kv_append, plus CB_ERR_TIMEOUT if a bounded wait expired.
+ */
+cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const void* v_pages,
+                                    const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                    const int32_t* kv_lens, int32_t block_size, float scale,
+                                    void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, const cb_dims* dims, void* stream);
+
+/*
+ * Options of cb_ragged_paged_attention_ex.  Zero-initialise for defaults.
+ *   decode_ctas   number of CTAs the decode pass spreads its key tiles over (0 = one per SM;
+ *                 1 forces every decode sequence into a single unsplit pass).  Results for
+ *                 different values agree within rounding; at most CB_MAX_DECODE_CTAS.
+ *   phase_events  NULL, or an array of CB_NUM_PHASE_EVENTS cudaEvent_t (created by the
+ *                 caller, passed as void*) that the call records on `stream` before the
+ *                 planner and after the planner, decode, merge and chunk kernels, so that
+ *                 cudaEventElapsedTime gives each kernel's device time.
+ */
+#define CB_NUM_PHASE_EVENTS 5
+typedef struct {
+  int32_t decode_ctas;
+  int32_t reserved0;
+  void* const* phase_events;
+  int64_t reserved[4];
+} cb_options;
+
+#define CB_MAX_DECODE_CTAS 512
+
+cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                       const int32_t* kv_lens, int32_t block_size, float scale,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, const cb_dims* dims,
+                                       const cb_options* options, void* stream);
+
+/*
+ * cb_get_device_error -- synchronise `stream`, then read and clear the current device's error
+ * word.  Returns CB_OK, CB_ERR_OUT_OF_RANGE, CB_ERR_TIMEOUT (reported first when both were
+ * seen) or CB_ERR_CUDA if the synchronisation itself failed.
+ */
+cb_status cb_get_device_error(void* stream);
+
+/* Static English name of a status code (never NULL). */
+const char* cb_status_string(cb_status status);
+
+/* Description of the last host-side error on the calling thread ("" if none). */
+const char* cb_last_error_message(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t cb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CB_H_ */

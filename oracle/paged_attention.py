@@ -139,10 +139,19 @@ def gather_kv(pages, table_row, kv_len: int, block_size: int) -> np.ndarray:
     bs = _check_block_size(block_size)
     P = pages.shape[0]
     flat = np.asarray(pages).reshape(P * bs, *pages.shape[2:])
-    slots = [slot_of(table_row, j, bs, P) for j in range(int(kv_len))]
-    if not slots:
+    n = int(kv_len)
+    if n == 0:
         return np.zeros((0,) + pages.shape[2:], dtype=np.float64)
-    return bf16_bits_to_f64(flat[np.asarray(slots)])
+    row = np.asarray(table_row, dtype=np.int64)
+    j = np.arange(n)
+    logical = j // bs
+    if logical[-1] >= row.shape[0]:
+        raise OracleError(f"kv_len {n} needs {logical[-1] + 1} blocks, table has {row.shape[0]}")
+    physical = row[logical]
+    if physical.min() < 0 or physical.max() >= P:
+        raise OracleError("block id outside the pool")
+    slots = physical * bs + j % bs   # the same rule as slot_of, for every key at once
+    return bf16_bits_to_f64(flat[slots])
 
 
 def stable_softmax(x: np.ndarray, axis: int = -1):

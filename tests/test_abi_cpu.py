@@ -1,0 +1,96 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol the header declares,
+and rejects bad host-side arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import continuous_batching_paged_gb300 as cb
+from continuous_batching_paged_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cb.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return cb.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("cb_kv_append", "cb_ragged_paged_attention", "cb_attention_workspace_size",
+                     "cb_get_device_error", "cb_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert cb.status_string(cb.CB_OK) == "CB_OK"
+    assert cb.status_string(cb.CB_ERR_OUT_OF_RANGE) == "CB_ERR_OUT_OF_RANGE"
+    assert cb.status_string(99) == "CB_ERR_UNKNOWN"
+    assert lib.cb_version() >= 100
+
+
+def _dims(**kw):
+    base = dict(num_seqs=4, num_tokens=35, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                num_pages=24, max_blocks_per_seq=9)
+    base.update(kw)
+    return cb.CbDims(**base)
+
+
+def test_workspace_size_is_host_arithmetic(lib):
+    n = lib.cb_attention_workspace_size(ctypes.byref(_dims()), 16)
+    assert n > 0 and n % 256 == 0
+    # grows with the number of sequences and heads, never with tokens or pages
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_seqs=400)), 16) > n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_tokens=9999, num_pages=999)), 16) == n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims()), 3) == 0       # block_size < 4
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(head_dim=96)), 16) == 0
+    assert lib.cb_attention_workspace_size(None, 16) == 0
+
+
+def _append_status(lib, dims, block_size, ptr=16):
+    p = ctypes.c_void_p(ptr)
+    return lib.cb_kv_append(p, p, p, p, p, p, p, block_size, ctypes.byref(dims), None)
+
+
+def test_host_validation_rejects_before_cuda(lib):
+    assert _append_status(lib, _dims(), 3) == cb.CB_ERR_INVALID_ARG
+    assert b"at least 4" in lib.cb_last_error_message()
+    assert _append_status(lib, _dims(num_q_heads=5), 16) == cb.CB_ERR_INVALID_ARG
+    assert _append_status(lib, _dims(head_dim=80), 16) == cb.CB_ERR_UNSUPPORTED
+    assert _append_status(lib, _dims(num_pages=0), 16) == cb.CB_ERR_INVALID_ARG
+    assert _append_status(lib, _dims(), 16, ptr=24) == cb.CB_ERR_INVALID_ARG   # misaligned
+    assert b"16-byte" in lib.cb_last_error_message()
+    # an empty batch is a valid no-op
+    assert _append_status(lib, _dims(num_tokens=0, num_seqs=0), 16) == cb.CB_OK
+    p = ctypes.c_void_p(256)
+    dims = _dims()
+    # workspace too small -> rejected before any launch
+    st = lib.cb_ragged_paged_attention(p, p, p, p, p, p, 16, 0.125, p, None, p, 256,
+                                       ctypes.byref(dims), None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"workspace" in lib.cb_last_error_message()
+    st = lib.cb_ragged_paged_attention(p, p, p, p, p, p, 16, -1.0, p, None, p, 1 << 30,
+                                       ctypes.byref(dims), None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"scale" in lib.cb_last_error_message()
+    st = lib.cb_ragged_paged_attention(p, p, p, p, None, p, 16, 0.125, p, None, p, 1 << 30,
+                                       ctypes.byref(dims), None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"null" in lib.cb_last_error_message()
+
+
+def test_build_flags_target_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)

@@ -1,0 +1,196 @@
+"""Ragged paged attention through the C ABI against the float64 oracle.
+
+Bar: every output element within 2e-2 + 1e-2 * |ref| (bf16 inputs, fp32 accumulation, bf16
+output); the softmax normaliser (lse) within 1e-3 + 1e-3 * |ref|; page permutation and prefix
+sharing give bit-identical GPU output (the kernels' split points depend only on lengths).
+"""
+import numpy as np
+import pytest
+import torch
+
+import continuous_batching_paged_gb300 as cb
+import workloads
+from gpu_util import DeviceBatch, named_config, assert_close, bits_of, bf16_tensor, i32, oracle_append
+from oracle import paged_attention as opa
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_full(b, decode_ctas=0):
+    """Append on the GPU, attend on the GPU, and compare every element with the oracle."""
+    db = DeviceBatch(b)
+    db.append()
+    out, lse = db.attend(lse=True, decode_ctas=decode_ctas)
+    assert cb.get_device_error() == cb.CB_OK
+    kp, vp = oracle_append(b)
+    ref, ref_lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
+                                              b.kv_lens, b.block_size, b.scale)
+    gpu = out.float().cpu().numpy()
+    assert_close(gpu, ref, b.name)
+    assert_close(lse.cpu().numpy(), ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
+    return db, out
+
+
+# ----------------------------------------------------------------------------- small, exhaustive
+
+def test_config1_tiny_ragged(cuda_lib):
+    _run_full(named_config(1))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [4, 16, 32, 64, 256])
+def test_decode_only_small(cuda_lib, D, bs):
+    kv = [1, 2, 15, 16, 17, 100, 257, 1000]
+    b = workloads.build_batch([1] * len(kv), kv, 8, 2, D, bs, seed=100 + bs + D,
+                              name=f"decode D{D} bs{bs}")
+    _run_full(b)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [4, 16, 64, 256])
+def test_chunks_small(cuda_lib, D, bs):
+    # chunks: ragged tails (130 = 128 + 2), prior context crossing tiles, a chunk at ctx 0
+    q_lens = [130, 2, 64, 257]
+    kv_lens = [130, 300, 64 + 77, 257 + 128]
+    b = workloads.build_batch(q_lens, kv_lens, 4, 2, D, bs, seed=200 + bs + D,
+                              name=f"chunks D{D} bs{bs}")
+    _run_full(b)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
+def test_mixed_gqa_groups(cuda_lib, G):
+    Hkv = 2 if G < 16 else 1
+    q_lens = [1, 40, 0, 1, 129, 1]
+    kv_lens = [33, 40, 12, 500, 129 + 200, 1]
+    b = workloads.build_batch(q_lens, kv_lens, Hkv * G, Hkv, 128, 32, seed=300 + G,
+                              name=f"mixed G{G}")
+    _run_full(b)
+
+
+def test_many_kv_heads_two_head_groups(cuda_lib):
+    b = workloads.build_batch([1, 1, 70], [300, 45, 170], 32, 16, 128, 16, seed=17,
+                              name="Hkv16")
+    _run_full(b)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 64, 512])
+def test_decode_split_counts_agree(cuda_lib, ctas):
+    kv = [3000, 17, 800, 4096, 1]
+    b = workloads.build_batch([1] * 5, kv, 32, 8, 128, 32, seed=23, name=f"splits{ctas}")
+    _run_full(b, decode_ctas=ctas)
+
+
+def test_max_table_length(cuda_lib):
+    bs = 64
+    mb = 40
+    b = workloads.build_batch([1, 200], [mb * bs, mb * bs], 16, 8, 128, bs, seed=31,
+                              max_blocks=mb, name="full table")
+    _run_full(b)
+
+
+def test_large_k_scale_softmax_range(cuda_lib):
+    b = workloads.build_batch([1, 300], [900, 1300], 8, 2, 128, 64, seed=41, k_scale=4.0,
+                              name="K x4")
+    _run_full(b)
+
+
+# ----------------------------------------------------------------------------- invariants
+
+def test_page_permutation_bit_identical(cuda_lib):
+    b = workloads.build_batch([1, 77, 1, 3], [400, 300, 64, 129], 8, 2, 128, 16, seed=51)
+    db, out = _run_full(b)
+    perm = np.random.default_rng(9).permutation(b.num_pages)
+    kp = torch.empty_like(db.k_pages)
+    vp = torch.empty_like(db.v_pages)
+    idx = torch.from_numpy(perm).cuda()
+    kp[idx] = db.k_pages
+    vp[idx] = db.v_pages
+    table = np.where(b.block_table >= 0, perm[np.maximum(b.block_table, 0)], -1)
+    out2 = db.attend(block_table=i32(table), k_pages=kp, v_pages=vp)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_shared_prefix_bit_identical_to_copies(cuda_lib):
+    b = workloads.build_batch([1, 1, 5], [200, 140, 133], 8, 2, 128, 16, seed=61,
+                              shared_prefix=([0, 1, 2], 128))
+    db, out = _run_full(b)
+    n_sh = 128 // 16
+    P = b.num_pages
+    kp = torch.cat([db.k_pages, torch.zeros((2 * n_sh,) + tuple(db.k_pages.shape[1:]),
+                                            dtype=db.k_pages.dtype, device="cuda")])
+    vp = torch.cat([db.v_pages, torch.zeros_like(kp[P:])])
+    table = b.block_table.copy()
+    for r, s in enumerate((1, 2)):
+        for j in range(n_sh):
+            new = P + r * n_sh + j
+            kp[new] = db.k_pages[int(table[s, j])]
+            vp[new] = db.v_pages[int(table[s, j])]
+            table[s, j] = new
+    out2 = db.attend(block_table=i32(table), k_pages=kp, v_pages=vp)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_empty_and_zero_length(cuda_lib):
+    b = workloads.build_batch([0, 2, 0], [5, 9, 0], 4, 2, 64, 16, seed=71)
+    _run_full(b)
+
+
+def test_bad_block_id_reported_without_fault(cuda_lib):
+    b = workloads.build_batch([1, 50], [70, 120], 8, 2, 128, 16, seed=81)
+    db = DeviceBatch(b)
+    db.append()
+    assert cb.get_device_error() == cb.CB_OK
+    table = b.block_table.copy()
+    table[0, 2] = 10 ** 6      # decode sequence
+    table[1, 3] = -5           # chunk sequence
+    db.attend(block_table=i32(table))
+    assert cb.get_device_error() == cb.CB_ERR_OUT_OF_RANGE
+    # the context is still usable
+    out = db.attend()
+    assert cb.get_device_error() == cb.CB_OK
+    assert torch.isfinite(out.float()).all()
+
+
+# ----------------------------------------------------------------------------- full-size configs
+
+def _sample_rows(b, rng, n_random=400):
+    q_lens = np.diff(b.cu_seqlens_q)
+    rows = set()
+    H = b.num_q_heads
+    for s in range(b.num_seqs):
+        c0 = int(b.cu_seqlens_q[s])
+        n = int(q_lens[s])
+        if n == 1:
+            rows.add((c0, int(rng.integers(H))))
+        elif n > 1:
+            for i in {0, 1, 127, 128, 129, n - 1, n - 2} & set(range(n)):
+                rows.add((c0 + i, int(rng.integers(H))))
+    T = b.num_tokens
+    for _ in range(n_random):
+        rows.add((int(rng.integers(T)), int(rng.integers(H))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_configs_full_size(cuda_lib, cfg):
+    b = named_config(cfg)
+    db = DeviceBatch(b)
+    db.append()
+    out, lse = db.attend(lse=True)
+    assert cb.get_device_error() == cb.CB_OK
+    gpu = out.float().cpu().numpy()
+    assert np.isfinite(gpu).all()
+    kp, vp = oracle_append(b)
+    if cfg in (2, 5):
+        ref, ref_lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
+                                                  b.kv_lens, b.block_size, b.scale)
+        assert_close(gpu, ref, b.name)
+        assert_close(lse.cpu().numpy(), ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
+    else:
+        rows = _sample_rows(b, np.random.default_rng(cfg))
+        ref, ref_lse = opa.attention_rows(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                          b.block_size, b.scale, rows)
+        t_idx = [t for t, _ in rows]
+        h_idx = [h for _, h in rows]
+        assert_close(gpu[t_idx, h_idx], ref, b.name)
+        assert_close(lse.cpu().numpy()[t_idx, h_idx], ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)

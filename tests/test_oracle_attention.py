@@ -328,3 +328,15 @@ def test_zero_length_sequences_are_noops():
     kp, vp = _appended(b)
     out, _ = _attend(b, kp, vp)
     assert out.shape == (3, 2, 8) and np.isfinite(out).all()
+
+
+def test_gather_matches_scalar_slot_rule():
+    b = workloads.make_config(1)
+    for s in range(b.num_seqs):
+        K = opa.gather_kv(b.k_pages, b.block_table[s], int(b.kv_lens[s]), b.block_size)
+        flat = b.k_pages.reshape(b.num_pages * b.block_size, *b.k_pages.shape[2:])
+        for j in range(int(b.kv_lens[s])):
+            slot = opa.slot_of(b.block_table[s], j, b.block_size, b.num_pages)
+            assert np.array_equal(K[j], _f64(flat[slot]), equal_nan=True)
+    with pytest.raises(OracleError):
+        opa.gather_kv(b.k_pages, b.block_table[0], 10 ** 4, b.block_size)

@@ -38,10 +38,21 @@ BF16_NAN = np.uint16(0x7FC0)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (round to nearest, ties to even); return the bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    out = rounded.astype(np.uint16)
+    """Round float32 values to bf16 (round to nearest, ties to even); return the bit patterns.
+
+    For finite inputs u + 0x7FFF + 1 stays below 2^32, so uint32 arithmetic is exact."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    flat_x = x.reshape(-1).view(np.uint32)
+    flat_o = out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, flat_x.size, step):
+        u = flat_x[i:i + step].copy()
+        lsb = (u >> 16) & 1
+        u += 0x7FFF
+        u += lsb
+        u >>= 16
+        flat_o[i:i + step] = u
     nan = np.isnan(x)
     if nan.any():
         out[nan] = BF16_NAN
@@ -87,10 +98,17 @@ class Batch:
 
 
 def _draw(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
-    x = rng.standard_normal(size=shape, dtype=np.float32)
-    if scale != 1.0:
-        x *= np.float32(scale)
-    return f32_to_bf16_bits(x)
+    """N(0, scale^2) values rounded to bf16, drawn in row-major order in chunks of 2^24."""
+    out = np.empty(shape, dtype=np.uint16)
+    flat = out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, flat.size, step):
+        n = min(step, flat.size - i)
+        x = rng.standard_normal(size=n, dtype=np.float32)
+        if scale != 1.0:
+            x *= np.float32(scale)
+        flat[i:i + n] = f32_to_bf16_bits(x)
+    return out
 
 
 def build_batch(
@@ -174,6 +192,7 @@ def build_batch(
     if referenced.size:
         k_pages[referenced] = _draw(rng, (referenced.size, bs, Hkv, D), k_scale)
         v_pages[referenced] = _draw(rng, (referenced.size, bs, Hkv, D))
+    # (referenced pages are drawn in ascending page-id order, K first, then V)
     # Poison every slot outside each sequence's prior context [0, ctx).  Shared
     # blocks are full prior context for all members, so this never touches them.
     for s in range(S):
