@@ -85,6 +85,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.cb_ragged_paged_attention.argtypes = attn + [_P]
     lib.cb_ragged_paged_attention_ex.restype = ctypes.c_int
     lib.cb_ragged_paged_attention_ex.argtypes = attn + [ctypes.POINTER(CbOptions), _P]
+    lib.cb_ragged_paged_attention_noalloc.restype = ctypes.c_int
+    lib.cb_ragged_paged_attention_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                                      ctypes.c_float, _P, _P,
+                                                      ctypes.POINTER(CbDims), _P]
     lib.cb_get_device_error.restype = ctypes.c_int
     lib.cb_get_device_error.argtypes = [_P]
 

@@ -127,6 +127,14 @@ cb_status encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
 
 }  // namespace
 
+namespace cb {
+// Record a host-side error for cb_last_error_message() from another translation unit.
+cb_status set_last_error(cb_status st, const char* msg) {
+  t_last_error = msg;
+  return st;
+}
+}  // namespace cb
+
 extern "C" {
 
 int32_t cb_version(void) { return 100; }

@@ -144,6 +144,31 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
                                        const cb_options* options, void* stream);
 
 /*
+ * cb_ragged_paged_attention_noalloc -- cb_ragged_paged_attention without a workspace argument.
+ * (An addition of this library with no counterpart in the pages that describe the method.)
+ *
+ * For callers that cannot allocate device memory: code that is handed only its input and
+ * output buffers by a host framework with no scratch allocator, or a steady-state serving loop
+ * that must not call cudaMalloc (which can synchronise the whole device).  The scratch comes
+ * from one fixed device array of CB_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library holds until the process exits.  The call allocates nothing.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other streams, or host
+ *     threads without ordering between them) race on it.  Each call rewrites every scratch
+ *     byte it later reads, so contents left by the previous call do no harm.
+ *   - A batch whose scratch need, cb_attention_workspace_size(dims, block_size), exceeds
+ *     CB_NOALLOC_SCRATCH_BYTES is rejected with CB_ERR_UNSUPPORTED before anything is queued.
+ * Arguments, results and errors are otherwise those of cb_ragged_paged_attention.
+ */
+#define CB_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+cb_status cb_ragged_paged_attention_noalloc(const void* q, const void* k_pages,
+                                            const void* v_pages, const int32_t* block_table,
+                                            const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                            int32_t block_size, float scale, void* out, float* lse,
+                                            const cb_dims* dims, void* stream);
+
+/*
  * cb_get_device_error -- synchronise `stream`, then read and clear the current device's error
  * word.  Returns CB_OK, CB_ERR_OUT_OF_RANGE, CB_ERR_TIMEOUT (reported first when both were
  * seen) or CB_ERR_CUDA if the synchronisation itself failed.
