@@ -488,7 +488,7 @@ def main():
         "config": workload_config(b, args),
         "e2e": {"value": world * b.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": (1 + 4) * args.steps,
+        "gpu_launches": 4 * args.steps,  # append, plan, decode (with merge), chunk
         "roofline": roof,
         "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
                    "gbs": dec_gbs, "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,

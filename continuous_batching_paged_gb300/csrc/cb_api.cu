@@ -271,8 +271,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   if (e == cudaSuccess && (e = cb::launch_decode(a, kmap, vmap, s)) != cudaSuccess)
     return cuda_fail(e, "decode launch");
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess && (e = cb::launch_merge(a, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
-  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess) e = mark(3);  // the merge runs inside the decode kernel
   if (e == cudaSuccess && (e = cb::launch_prefill(a, qmap, kmap, vmap, s)) != cudaSuccess)
     return cuda_fail(e, "prefill launch");
   if (e == cudaSuccess) e = mark(4);

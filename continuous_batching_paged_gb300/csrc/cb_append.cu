@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
         v[1] = (kv + kDecodeTileKeys - 1) / kDecodeTileKeys;
       } else if (q_len > 1) {
         v[2] = 1;
-        v[3] = (q_len + kPrefillTileM - 1) / kPrefillTileM;
+        v[3] = (q_len + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);  // pairs of query tiles
       }
     }
     int ex[4], tot[4];
@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   const long long ntiles = carry[1];
   const int N = (int)(ntiles < a.decode_ctas ? (ntiles > 0 ? ntiles : 1) : a.decode_ctas);
   if (tid == 0) hdr->decode_ctas = N;
+  // Merge counters of the decode pass: one per (decode sequence, KV head), zero at start.
+  int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
+  for (int i = tid; i < n_dec * a.Hkv; i += kPlanThreads) merge_cnt[i] = 0;
   for (int c = tid; c <= N; c += kPlanThreads) {
     const long long t0 = ntiles * c / N;
     int lo = 0, hi = n_dec;  // largest d in [0, n_dec] with dec_prefix[d] <= t0

@@ -28,7 +28,7 @@ struct PlanHeader {
   int32_t n_dec;          // number of decode sequences (q_len == 1)
   int32_t dec_tiles;      // total 16-key tiles over all decode sequences
   int32_t n_pf;           // number of chunk sequences (q_len > 1)
-  int32_t pf_qtiles;      // total 128-query tiles over all chunk sequences
+  int32_t pf_qtiles;      // total pairs of 128-query tiles over all chunk sequences
   int32_t pf_counter;     // dynamic work counter of the prefill pass (reset by the planner)
   int32_t decode_ctas;    // CTAs the decode pass was planned for
   int32_t pad[10];
@@ -36,7 +36,8 @@ struct PlanHeader {
 
 // Byte offsets of the workspace sections (all 256-byte aligned).
 struct WsLayout {
-  size_t header, dec_seq, dec_prefix, cta_first, pf_seq, pf_prefix, part_ml, part_o, total;
+  size_t header, dec_seq, dec_prefix, cta_first, pf_seq, pf_prefix, merge_cnt, part_ml, part_o,
+      total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -50,6 +51,7 @@ __host__ __device__ inline WsLayout ws_layout(int S, int Hq, int D) {
   L.cta_first = off;  off = align_up(off + sizeof(int32_t) * (size_t)(CB_MAX_DECODE_CTAS + 1), 256);
   L.pf_seq = off;     off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
   L.pf_prefix = off;  off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
+  L.merge_cnt = off;  off = align_up(off + sizeof(int32_t) * (size_t)S * (size_t)Hq, 256);
   const size_t slots = (size_t)CB_MAX_DECODE_CTAS + (size_t)S;
   L.part_ml = off;    off = align_up(off + sizeof(float2) * slots * (size_t)Hq, 256);
   L.part_o = off;     off = align_up(off + sizeof(float) * slots * (size_t)Hq * (size_t)D, 256);
@@ -161,6 +163,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // with the 128-byte swizzle: the chunk index is XORed with the row index modulo 8.
 __device__ __forceinline__ uint32_t sw128(uint32_t region, uint32_t row, uint32_t chunk) {
   return region + row * 128u + (((chunk ^ row) & 7u) << 4);
+}
+
+// Register reallocation between warpgroups (all four warps of a warpgroup execute it).  The
+// counts handed out must add up to no more than what the block was launched with.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------------------------------

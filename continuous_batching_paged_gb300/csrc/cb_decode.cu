@@ -5,9 +5,10 @@
 //
 //   * The key tiles of all decode sequences are laid end to end (16 keys per tile) and cut into
 //     `decode_ctas` equal contiguous ranges, one per CTA: every CTA streams the same number of
-//     bytes whatever the length mix.  A sequence cut by a range boundary is finished by the
-//     merge kernel from per-CTA partial results (m, l, o): the split-KV scheme with an online
-//     softmax and a log-sum-exp merge.
+//     bytes whatever the length mix.  A sequence cut by range boundaries leaves per-CTA partial
+//     results (m, l, o) in the workspace; the last warp to finish a (sequence, KV head) merges
+//     them (an atomic counter per pair decides which): the split-KV scheme with an online
+//     softmax and a log-sum-exp merge, without a separate merge launch.
 //   * One producer warp walks the range, prefetches block-table entries 32 at a time, and
 //     issues TMA tensor copies (128-byte swizzle) of each (page run, KV head, 64-wide half of D)
 //     into a multi-stage shared-memory ring guarded by mbarriers.
@@ -33,7 +34,7 @@ struct StageInfo {
   int kv;        // kv_len
   int key0;      // first key of this tile
   uint32_t flags;
-  int pad[2];
+  int p0, p1;    // the sequence's tile range [p0, p1) in the concatenated tile order
 };
 
 template <int D>
@@ -55,6 +56,42 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
     if (n * mid / N <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// One warp combines the partial (m, l, o) that CTAs cf..cl wrote for decode sequence `dec`
+// and KV head `kvh` (its G query heads): M = max m_c, w_c = 2^(m_c - M),
+// out = sum_c w_c o_c / sum_c w_c l_c, lse = (M + log2 sum_c w_c l_c) * ln 2.
+template <int D>
+__device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* part_ml,
+                                            const float* part_o, int dec, int tok, int kvh,
+                                            int cf, int cl, int lane) {
+  constexpr int PER = D / 32;  // output columns per lane
+  __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
+  for (int r = 0; r < a.G; ++r) {
+    const int head = kvh * a.G + r;
+    // Other CTAs wrote these parts: read them through L2 (ld.global.cg), never a stale L1 line.
+    float M = -INFINITY;
+    for (int cc = cf; cc <= cl; ++cc)
+      M = fmaxf(M, __ldcg(part_ml + ((size_t)cc + dec) * a.Hq + head).x);
+    float Lsum = 0.f, acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    for (int cc = cf; cc <= cl; ++cc) {
+      const size_t slot = (size_t)cc + dec;
+      const float2 ml = __ldcg(part_ml + slot * a.Hq + head);
+      const float w = fast_exp2(ml.x - M);
+      Lsum += ml.y * w;
+      const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += __ldcg(po + i) * w;
+    }
+    const float inv = 1.f / Lsum;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
+#pragma unroll
+    for (int i = 0; i < PER / 2; ++i) dst[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    if (lane == 0 && a.lse != nullptr)
+      a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
+  }
 }
 
 template <int D>
@@ -159,6 +196,8 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             si.tok = tok;
             si.kv = kv;
             si.key0 = key0;
+            si.p0 = (int)p0;
+            si.p1 = (int)p1;
             si.flags = (tile == lo ? kInfoFirst : 0u) | (tile == hi - 1 ? kInfoLast : 0u) |
                        (complete ? kInfoComplete : 0u);
             mbar_arrive_expect_tx(bar_full + 8 * stage,
@@ -199,6 +238,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
     (void)dummy;
     float2* part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml);
     float* part_o = reinterpret_cast<float*>(a.ws + L.part_o);
+    int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
     __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
 
@@ -366,48 +406,21 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             if (tq == 0) part_ml[slot * a.Hq + head] = make_float2(ms[hr], ls[hr]);
           }
         }
+        if (!(si.flags & kInfoComplete)) {
+          // Split sequence: the last warp to finish this (sequence, KV head) merges all parts.
+          const int cf = cta_of_tile(si.p0, ntiles, N), cl = cta_of_tile(si.p1 - 1, ntiles, N);
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == cl - cf;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) {
+            __threadfence();
+            merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, lane);
+          }
+        }
       }
     }
-  }
-}
-
-// Combine the partial (m, l, o) of decode sequences whose tiles span several CTAs.
-__global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a) {
-  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
-  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
-  const int d = blockIdx.x;
-  if (d >= hdr->n_dec) return;
-  const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
-  const int32_t* dec_prefix = reinterpret_cast<const int32_t*>(a.ws + L.dec_prefix);
-  const float2* part_ml = reinterpret_cast<const float2*>(a.ws + L.part_ml);
-  const float* part_o = reinterpret_cast<const float*>(a.ws + L.part_o);
-  const long long n = hdr->dec_tiles;
-  const int N = hdr->decode_ctas;
-  const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
-  const int cf = cta_of_tile(p0, n, N), cl = cta_of_tile(p1 - 1, n, N);
-  if (cf == cl) return;  // written directly by the decode pass
-  const int s = dec_seq[d];
-  const int tok = a.cu_seqlens_q[s];
-  __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
-  for (int idx = threadIdx.x; idx < a.Hq * a.D; idx += blockDim.x) {
-    const int head = idx / a.D, dd = idx % a.D;
-    float M = -INFINITY;
-    for (int cc = cf; cc <= cl; ++cc) {
-      if (n * cc / N == n * (cc + 1) / N) continue;  // empty range: wrote no partial
-      M = fmaxf(M, part_ml[((size_t)cc + d) * a.Hq + head].x);
-    }
-    float Lsum = 0.f, O = 0.f;
-    for (int cc = cf; cc <= cl; ++cc) {
-      if (n * cc / N == n * (cc + 1) / N) continue;
-      const size_t slot = (size_t)cc + d;
-      const float2 ml = part_ml[slot * a.Hq + head];
-      const float w = fast_exp2(ml.x - M);
-      Lsum += ml.y * w;
-      O += part_o[(slot * a.Hq + head) * a.D + dd] * w;
-    }
-    outg[((size_t)tok * a.Hq + head) * a.D + dd] = __float2bfloat16_rn(O / Lsum);
-    if (dd == 0 && a.lse != nullptr)
-      a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
   }
 }
 
@@ -434,12 +447,6 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
                           cudaStream_t stream) {
   if (a.D == 128) return launch_decode_d<128>(a, kmap, vmap, stream);
   return launch_decode_d<64>(a, kmap, vmap, stream);
-}
-
-cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
-  if (a.S == 0) return cudaSuccess;
-  merge_kernel<<<a.S, 256, 0, stream>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace cb

@@ -39,7 +39,6 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
-cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream);
 

@@ -4,21 +4,28 @@
 // cores.  A chunk of queries attends to a cache that already holds the earlier chunks: query i
 // of a chunk with prior context ctx sees keys 0 .. ctx + i (same section).
 //
-// One work item = (chunk sequence, 128-query tile, query head).  Persistent CTAs (one per SM)
-// take items from a device counter the planner reset.  Per CTA, warp-specialised:
-//   warp 0      TMA producer: the Q tile once per item, then K and V tiles of 128 keys gathered
-//               page run by page run through the block table into a 2-stage smem ring
-//               (128-byte swizzle, the layout the tensor core descriptors read directly).
-//   warp 1      tcgen05 issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_j V_j with P_j read from TMEM; completion is signalled through
+// One work item = (chunk sequence, pair of 128-query tiles A and B, query head).  Persistent
+// CTAs (one per SM) take items from a device counter the planner reset; items are ordered
+// longest first within a chunk and with the query head fastest, so the CTAs working on the
+// heads of one KV group at the same time share its K/V tiles through L2.  Per CTA,
+// warp-specialised (12 warps, three warpgroups; setmaxnreg moves registers from the first
+// warpgroup, which only issues copies and MMAs, to the two softmax warpgroups: 104 + 2 x 200
+// per thread slot = the 3 x 168 the launch provides):
+//   warp 0      TMA producer: Q tiles A and B once per item, then the K and V tiles of 128 keys
+//               gathered page run by page run through the block table into a 2-stage ring
+//               (128-byte swizzle: the layout the tensor-core descriptors read directly).
+//   warp 1      tcgen05 issuer (one thread): for each K/V tile j, S_A = Q_A K_j^T and
+//               S_B = Q_B K_j^T into TMEM; then O_A += P_A V_j and O_B += P_B V_j with P read
+//               from TMEM, interleaved with the next tile's S so the tensor core always has the
+//               other tile's work while one softmax group runs.  Completion is signalled with
 //               tcgen05.commit on mbarriers.  Also owns the TMEM allocation.
-//   warps 2-5   softmax: thread r owns query row r (TMEM lane r); it loads its 128 scores
-//               with tcgen05.ld, applies the causal mask only on tiles that cross the diagonal,
-//               keeps the running max m and sum l in registers, writes P (bf16) back over S,
-//               and rescales O in TMEM only when m grows by more than 2^8 (otherwise the stale
-//               max keeps every p <= 256, which fp32 and bf16 represent exactly as well); the
-//               final O / l is written as bf16.
-// TMEM columns: [0,128) S/P buffer 0, [128,256) S/P buffer 1, [256, 256+D) O.
+//   warps 4-7   softmax group A, warps 8-11 softmax group B: thread r owns query row r (TMEM
+//               lane r) of its tile; it loads its 128 scores with tcgen05.ld, applies the causal
+//               mask only on tiles that cross the diagonal, keeps the running max m and sum l in
+//               registers (tree reductions), writes P (bf16) back over S, rescales O in TMEM
+//               only when m grows by more than 8 in log2 units (otherwise the stale max keeps
+//               every p <= 2^8, exact enough in fp32 and bf16), and writes O / l as bf16.
+// TMEM columns: [0,128) S/P of A, [128,256) S/P of B, [256,256+D) O of A, then O of B.
 #include "cb_common.cuh"
 #include "cb_launch.h"
 
@@ -28,51 +35,67 @@ template <int D>
 struct PrefillSmem {
   static constexpr int kHalves = D / 64;
   static constexpr int kHalfBytes = 128 * 128;             // 128 rows of 128 B
-  static constexpr int kTileBytes = kHalves * kHalfBytes;  // a Q, K or V tile
+  static constexpr int kTileBytes = kHalves * kHalfBytes;  // one Q, K or V tile
   static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kQ = 0;
-  static constexpr int kStage0 = kTileBytes;               // stage i: K at +0, V at +kTileBytes
+  static constexpr int kQ0 = 0;                            // Q_A, then Q_B
+  static constexpr int kStage0 = 2 * kTileBytes;           // stage i: K at +0, V at +kTileBytes
   static constexpr int kBar = kStage0 + kStages * 2 * kTileBytes;
-  // barrier indices (8 bytes each)
+  // barrier indices (8 bytes each); [2] arrays are indexed by the tile (A = 0, B = 1)
   static constexpr int bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = bKFull + kStages,
-                       bKVEmpty = bVFull + kStages, bSFull = bKVEmpty + kStages,
-                       bPFull = bSFull + 2, bODone = bPFull + 2, bOFree = bODone + 1,
-                       bItemFull = bOFree + 1, bItemEmpty = bItemFull + 2,
+                       bKEmpty = bVFull + kStages, bVEmpty = bKEmpty + kStages,
+                       bSFull = bVEmpty + kStages,
+                       bPFull = bSFull + 2, bODone = bPFull + 2, bOFree = bODone + 2,
+                       bItemFull = bOFree + 2, bItemEmpty = bItemFull + 2,
                        kNumBars = bItemEmpty + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;        // tmem base, item ids
   static constexpr int kTotal = kMisc + 64 + 1024;
 };
 
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPrefillThreads = 192;
+constexpr int kPrefillThreads = 384;
+constexpr int kRegsIssue = 104;    // warpgroup 0 (producer, MMA issuer, two idle warps)
+constexpr int kRegsSoftmax = 200;  // warpgroups 1 and 2
+static_assert(kRegsIssue + 2 * kRegsSoftmax <= 3 * 168, "register split exceeds the launch");
+constexpr int kItemConsumers = 9;  // MMA thread + 4 warps of each softmax group
 
 struct PfItem {
-  int s, tok0, rows, ctx, head, kvh, qt, n_keys, n_tiles;
+  int s, head, kvh, ctx;
+  int tok[2], rows[2], nk[2], nt[2];  // per tile: first token, valid rows, keys, K/V tiles
+  int nt_all, nk_all;                 // K/V tiles loaded and keys covered for the pair
+  bool hasB;
 };
 
 __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
                                                  const int32_t* pf_seq, const int32_t* pf_prefix,
                                                  int n_pf) {
   PfItem it;
-  const int qtg = item / a.Hq;
-  it.head = item - qtg * a.Hq;
+  const int pg = item / a.Hq;  // global pair index
+  it.head = item - pg * a.Hq;
   it.kvh = it.head / a.G;
-  int lo = 0, hi = n_pf - 1;  // largest i with pf_prefix[i] <= qtg
+  int lo = 0, hi = n_pf - 1;  // largest i with pf_prefix[i] <= pg
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pf_prefix[mid] <= qtg) lo = mid; else hi = mid - 1;
+    if (pf_prefix[mid] <= pg) lo = mid; else hi = mid - 1;
   }
   it.s = pf_seq[lo];
   const int c0 = a.cu_seqlens_q[it.s];
   const int q_len = a.cu_seqlens_q[it.s + 1] - c0;
-  const int kv = a.kv_lens[it.s];
-  it.ctx = kv - q_len;
-  const int nqt = pf_prefix[lo + 1] - pf_prefix[lo];
-  it.qt = nqt - 1 - (qtg - pf_prefix[lo]);  // longest tiles of a chunk first
-  it.rows = min(kPrefillTileM, q_len - it.qt * kPrefillTileM);
-  it.tok0 = c0 + it.qt * kPrefillTileM;
-  it.n_keys = it.ctx + it.qt * kPrefillTileM + it.rows;
-  it.n_tiles = (it.n_keys + kPrefillTileN - 1) / kPrefillTileN;
+  it.ctx = a.kv_lens[it.s] - q_len;
+  const int npairs = pf_prefix[lo + 1] - pf_prefix[lo];
+  const int p = npairs - 1 - (pg - pf_prefix[lo]);  // longest pairs of a chunk first
+  const int nqt = (q_len + kPrefillTileM - 1) / kPrefillTileM;
+  const int tA = 2 * p, tB = 2 * p + 1;
+  it.hasB = tB < nqt;
+  it.tok[0] = c0 + tA * kPrefillTileM;
+  it.tok[1] = it.tok[0] + kPrefillTileM;
+  it.rows[0] = min(kPrefillTileM, q_len - tA * kPrefillTileM);
+  it.rows[1] = it.hasB ? min(kPrefillTileM, q_len - tB * kPrefillTileM) : 0;
+  it.nk[0] = it.ctx + tA * kPrefillTileM + it.rows[0];
+  it.nk[1] = it.hasB ? it.ctx + tB * kPrefillTileM + it.rows[1] : 0;
+  it.nt[0] = (it.nk[0] + kPrefillTileN - 1) / kPrefillTileN;
+  it.nt[1] = (it.nk[1] + kPrefillTileN - 1) / kPrefillTileN;
+  it.nk_all = max(it.nk[0], it.nk[1]);
+  it.nt_all = max(it.nt[0], it.nt[1]);
   return it;
 }
 
@@ -97,7 +120,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int32_t* pf_seq = reinterpret_cast<const int32_t*>(a.ws + L.pf_seq);
   const int32_t* pf_prefix = reinterpret_cast<const int32_t*>(a.ws + L.pf_prefix);
   const int n_pf = hdr->n_pf;
-  const int n_items = hdr->pf_qtiles * a.Hq;
+  const int n_items = hdr->pf_qtiles * a.Hq;  // pf_qtiles counts tile pairs
   if (n_items == 0) return;
 
   if (threadIdx.x == 0) {
@@ -106,16 +129,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int i = 0; i < NS; ++i) {
       mbar_init(bar(SM::bKFull + i), 1);
       mbar_init(bar(SM::bVFull + i), 1);
-      mbar_init(bar(SM::bKVEmpty + i), 1);
+      mbar_init(bar(SM::bKEmpty + i), 1);
+      mbar_init(bar(SM::bVEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SM::bSFull + i), 1);
       mbar_init(bar(SM::bPFull + i), 128);
+      mbar_init(bar(SM::bODone + i), 1);
+      mbar_init(bar(SM::bOFree + i), 128);
       mbar_init(bar(SM::bItemFull + i), 1);
-      mbar_init(bar(SM::bItemEmpty + i), 5);
+      mbar_init(bar(SM::bItemEmpty + i), kItemConsumers);
     }
-    mbar_init(bar(SM::bODone), 1);
-    mbar_init(bar(SM::bOFree), 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -127,7 +151,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  // Each role runs inside the branch that set its register count (no join in between, so the
+  // compiler allocates every role's code under that role's own limit).
+  if (warp < 4) {
+    regs_dec<kRegsIssue>();
+    if (warp == 0) {
     // ===================================================================== TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
@@ -152,14 +180,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
       if (lane == 0) {
         if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
-        mbar_arrive_expect_tx(bar(SM::bQFull), SM::kTileBytes);
+        mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kTileBytes);
+        for (int t = 0; t < (it.hasB ? 2 : 1); ++t)
 #pragma unroll
-        for (int half = 0; half < SM::kHalves; ++half)
-          tma_load_3d(sbase + SM::kQ + half * SM::kHalfBytes, &qmap, bar(SM::bQFull), half * 64,
-                      it.head, it.tok0);
+          for (int half = 0; half < SM::kHalves; ++half)
+            tma_load_3d(sbase + SM::kQ0 + t * SM::kTileBytes + half * SM::kHalfBytes, &qmap,
+                        bar(SM::bQFull), half * 64, it.head, it.tok[t]);
       }
       const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
-      for (int j = 0; j < it.n_tiles; ++j, ++g) {
+      for (int j = 0; j < it.nt_all; ++j, ++g) {
         const int stage = g % NS;
         const uint32_t phase = (g / NS) & 1;
         const int key0 = j * kPrefillTileN;
@@ -171,7 +200,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           const int sb = p * 32 + lane;
           const int pos = key0 + sb * KB;
           ent[p] = -1;
-          if (sb < nsb && pos < it.n_keys) {
+          if (sb < nsb && pos < it.nk_all) {
             const int lb = pos / a.bs;
             ent[p] = lb < a.max_blocks ? __ldg(row + lb) : -2;
           }
@@ -180,32 +209,35 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
           const int sb = p * 32 + lane;
-          const bool want = sb < nsb && key0 + sb * KB < it.n_keys;
+          const bool want = sb < nsb && key0 + sb * KB < it.nk_all;
           const bool valid = want && ent[p] >= 0 && ent[p] < a.P;
           if (want && !valid) report(a.err, kErrOutOfRange);
           nvalid += __popc(__ballot_sync(0xffffffffu, valid));
         }
-        if (lane == 0) {
-          if (!mbar_wait(bar(SM::bKVEmpty + stage), phase ^ 1)) report(a.err, kErrTimeout);
-          const uint32_t bytes = nvalid * (uint32_t)(SM::kHalves * KB * 128);
-          mbar_arrive_expect_tx(bar(SM::bKFull + stage), bytes);
-          mbar_arrive_expect_tx(bar(SM::bVFull + stage), bytes);
-        }
-        __syncwarp();
+        const uint32_t bytes = nvalid * (uint32_t)(SM::kHalves * KB * 128);
         const uint32_t kst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes;
         const uint32_t vst = kst + SM::kTileBytes;
+        // K and V of a stage are released separately: K once both S products of its tile are
+        // done, V once both PV products are.
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv) {
+          if (lane == 0) {
+            if (!mbar_wait(bar((kv ? SM::bVEmpty : SM::bKEmpty) + stage), phase ^ 1))
+              report(a.err, kErrTimeout);
+            mbar_arrive_expect_tx(bar((kv ? SM::bVFull : SM::bKFull) + stage), bytes);
+          }
+          __syncwarp();
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int sb = p * 32 + lane;
-          const int pos = key0 + sb * KB;
-          if (sb < nsb && pos < it.n_keys && ent[p] >= 0 && ent[p] < a.P) {
-            const int token = ent[p] * a.bs + (pos % a.bs);
+          for (int p = 0; p < 4; ++p) {
+            const int sb = p * 32 + lane;
+            const int pos = key0 + sb * KB;
+            if (sb < nsb && pos < it.nk_all && ent[p] >= 0 && ent[p] < a.P) {
+              const int token = ent[p] * a.bs + (pos % a.bs);
 #pragma unroll
-            for (int half = 0; half < SM::kHalves; ++half) {
-              tma_load_3d(kst + half * SM::kHalfBytes + sb * KB * 128, &kmap,
-                          bar(SM::bKFull + stage), half * 64, it.kvh, token);
-              tma_load_3d(vst + half * SM::kHalfBytes + sb * KB * 128, &vmap,
-                          bar(SM::bVFull + stage), half * 64, it.kvh, token);
+              for (int half = 0; half < SM::kHalves; ++half)
+                tma_load_3d((kv ? vst : kst) + half * SM::kHalfBytes + sb * KB * 128,
+                            kv ? &vmap : &kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
+                            half * 64, it.kvh, token);
             }
           }
         }
@@ -216,65 +248,93 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kPrefillTileM, kPrefillTileN, 0);
       constexpr uint32_t idesc_o = idesc_bf16(kPrefillTileM, D, 1);
-      const uint32_t t_o = tmem + 256;
-      uint32_t g = 0;
+      uint32_t g = 0, gx[2] = {0, 0}, kx[2] = {0, 0};
       bool ok = true;
-      auto issue_s = [&](uint32_t gg) {
+      auto wait = [&](uint32_t b, uint32_t parity) {
+        if (ok && !mbar_wait(b, parity)) {
+          report(a.err, kErrTimeout);
+          ok = false;
+        }
+      };
+      // Descriptor of the first 16-wide K slice of each operand region; a slice at byte offset
+      // `off` is the same descriptor with (off >> 4) added to its start-address field.
+      const uint64_t q_desc0 = smem_desc_sw128(sbase + SM::kQ0, 16, 1024);
+      const uint64_t kv_desc0 = smem_desc_sw128(sbase + SM::kStage0, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + SM::kStage0 + SM::kTileBytes,
+                                               SM::kHalfBytes, 1024);
+      // S_t = Q_t K^T for K/V tile gg into tile t's S buffer.
+      auto issue_s = [&](int t, uint32_t gg) {
         const int stage = gg % NS;
-        if (!mbar_wait(bar(SM::bKFull + stage), (gg / NS) & 1)) { report(a.err, kErrTimeout); ok = false; }
+        wait(bar(SM::bKFull + stage), (gg / NS) & 1);
         tc_fence_after();
-        const uint32_t kst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes;
-        const uint32_t d_s = tmem + (gg & 1) * 128;
+        const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kTileBytes) >> 4);
+        const uint64_t kd = kv_desc0 + ((uint32_t)(stage * 2 * SM::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * SM::kHalfBytes + (kk & 3) * 32;
-          tc_mma_ss(d_s, smem_desc_sw128(sbase + SM::kQ + off, 16, 1024),
-                    smem_desc_sw128(kst + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * SM::kHalfBytes + (kk & 3) * 32) >> 4;
+          tc_mma_ss(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(SM::bSFull + (gg & 1)));
+        tc_commit(bar(SM::bSFull + t));
       };
       for (uint32_t k = 0; ok; ++k) {
         const int slot = k & 1;
-        if (!mbar_wait(bar(SM::bItemFull + slot), (k >> 1) & 1)) { report(a.err, kErrTimeout); break; }
+        wait(bar(SM::bItemFull + slot), (k >> 1) & 1);
+        if (!ok) break;
         const int item = item_ids[slot];
         mbar_arrive(bar(SM::bItemEmpty + slot));
         if (item < 0) break;
         const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
-        if (!mbar_wait(bar(SM::bQFull), k & 1)) { report(a.err, kErrTimeout); break; }
+        const int nt_t[2] = {it.nt[0], it.hasB ? it.nt[1] : 0};
+        wait(bar(SM::bQFull), k & 1);
         tc_fence_after();
-        issue_s(g);
-        for (int j = 0; j < it.n_tiles && ok; ++j) {
+        issue_s(0, g);
+        if (nt_t[1] > 0) issue_s(1, g);
+        tc_commit(bar(SM::bKEmpty + g % NS));
+        for (int j = 0; j < it.nt_all && ok; ++j) {
           const uint32_t gj = g + j;
-          if (j + 1 < it.n_tiles) issue_s(gj + 1);
-          else tc_commit(bar(SM::bQEmpty));
-          if (!mbar_wait(bar(SM::bPFull + (gj & 1)), (gj >> 1) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
           const int stage = gj % NS;
-          if (!mbar_wait(bar(SM::bVFull + stage), (gj / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
-          if (j == 0 && k > 0) {
-            if (!mbar_wait(bar(SM::bOFree), (k - 1) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
-          }
-          tc_fence_after();
-          const uint32_t vst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes + SM::kTileBytes;
-          const uint32_t p_t = tmem + (gj & 1) * 128;
+          wait(bar(SM::bVFull + stage), (gj / NS) & 1);
+          const uint64_t vd = v_desc0 + ((uint32_t)(stage * 2 * SM::kTileBytes) >> 4);
+#pragma unroll 1
+          for (int t = 0; t < 2; ++t) {
+            if (j >= nt_t[t]) continue;
+            wait(bar(SM::bPFull + t), (gx[t] + j) & 1);
+            if (j == 0 && kx[t] > 0) wait(bar(SM::bOFree + t), (kx[t] - 1) & 1);
+            tc_fence_after();
+            const uint32_t p_t = tmem + t * 128;
+            const uint32_t o_t = tmem + 256 + t * D;
 #pragma unroll
-          for (int kk = 0; kk < kPrefillTileN / 16; ++kk) {
-            tc_mma_ts(t_o, p_t + kk * 8, smem_desc_sw128(vst + kk * 2048, SM::kHalfBytes, 1024),
-                      idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kPrefillTileN / 16; ++kk)
+              tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+            if (j == nt_t[t] - 1) tc_commit(bar(SM::bODone + t));
+            if (j + 1 < nt_t[t]) issue_s(t, gj + 1);
           }
-          tc_commit(bar(SM::bODone));
-          tc_commit(bar(SM::bKVEmpty + stage));
+          tc_commit(bar(SM::bVEmpty + stage));
+          if (j + 1 < it.nt_all) tc_commit(bar(SM::bKEmpty + (gj + 1) % NS));
+          if (j == it.nt_all - 1) tc_commit(bar(SM::bQEmpty));
         }
-        g += it.n_tiles;
+        g += it.nt_all;
+        for (int t = 0; t < 2; ++t) {
+          if (nt_t[t] > 0) {
+            gx[t] += nt_t[t];
+            kx[t] += 1;
+          }
+        }
       }
     }
+    }
   } else {
-    // ===================================================================== softmax warps
+    regs_inc<kRegsSoftmax>();
+    // ===================================================================== softmax groups
+    const int t = (warp - 4) >> 2;                // 0: tile A, 1: tile B
     const int quad = warp & 3;                    // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;               // query row within the tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t s_col = t * 128, o_col = 256 + t * D;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
-    uint32_t g = 0;
+    uint32_t g = 0, gx = 0, kx = 0;
     for (uint32_t k = 0;; ++k) {
       const int slot = k & 1;
       if (!mbar_wait(bar(SM::bItemFull + slot), (k >> 1) & 1)) { report(a.err, kErrTimeout); break; }
@@ -283,34 +343,38 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
       if (item < 0) break;
       const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
-      const int limit = it.ctx + it.qt * kPrefillTileM + r;       // last key row r may see
-      const int diag0 = it.ctx + it.qt * kPrefillTileM;           // row 0's last key
+      const uint32_t g_item = g;
+      g += it.nt_all;
+      if (t == 1 && !it.hasB) continue;
+      const int nt = it.nt[t];
+      const int diag0 = it.ctx + (it.tok[t] - a.cu_seqlens_q[it.s]);  // row 0's last key
+      const int limit = diag0 + r;                     // row r's last visible key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      for (int j = 0; j < it.n_tiles; ++j) {
-        const uint32_t gj = g + j;
-        const uint32_t buf = gj & 1;
-        if (!mbar_wait(bar(SM::bSFull + buf), (gj >> 1) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t gj = gx + j;
+        if (!mbar_wait(bar(SM::bSFull + t), gj & 1)) { report(a.err, kErrTimeout); ok = false; break; }
         __syncwarp();
         tc_fence_after();
         uint32_t sr[128];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + buf * 128 + i * 32, sr + i * 32);
+        for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + s_col + i * 32, sr + i * 32);
         tc_wait_ld();
         const int key0 = j * kPrefillTileN;
-        float mx = -INFINITY;
         if (key0 + kPrefillTileN - 1 > diag0) {
 #pragma unroll
-          for (int cidx = 0; cidx < 128; ++cidx) {
-            float v = __uint_as_float(sr[cidx]);
-            v = (key0 + cidx <= limit) ? v : -INFINITY;
-            sr[cidx] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-        } else {
-#pragma unroll
-          for (int cidx = 0; cidx < 128; ++cidx) mx = fmaxf(mx, __uint_as_float(sr[cidx]));
+          for (int c = 0; c < 128; ++c)
+            if (key0 + c > limit) sr[c] = __float_as_uint(-INFINITY);
         }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sr[i]);
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], __uint_as_float(sr[c + i]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float mt = mx * sl2;
         float alpha = 1.f;
         bool resc = false;
@@ -321,38 +385,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           m_run = mt;
           resc = true;
         }
-        float sum = 0.f;
+        float sm8[8];
 #pragma unroll
-        for (int cidx = 0; cidx < 128; cidx += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[cidx]), sl2, -m_run));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[cidx + 1]), sl2, -m_run));
-          sum += p0 + p1;
-          sr[cidx >> 1] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 8; ++i) sm8[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_run));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_run));
+          sm8[(c >> 1) & 7] += p0 + p1;
+          sr[c >> 1] = pack_bf16x2(p0, p1);
         }
+        const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
         l_run = l_run * alpha + sum;
-        if (__any_sync(0xffffffffu, resc)) {
-          // O holds PV_{j-1}: wait for it, then scale this warp's 32 rows in place.
-          if (!mbar_wait(bar(SM::bODone), (gj - 1) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
-          __syncwarp();
-          tc_fence_after();
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t ov[32];
-            tmem_ld32(t_lane + 256 + ch * 32, ov);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_lane + 256 + ch * 32, ov);
-          }
-          tc_wait_st();
-        }
-        if (j == it.n_tiles - 1) {
-          // Keys at or past n_keys in the last tile: their V rows hold stale or poison data and
-          // P is 0 there, but 0 * NaN is NaN, so zero them before the PV product reads them.
-          const int stage = gj % NS;
-          const int first = it.n_keys - key0;  // 1..128
+        if (j == it.nt_all - 1) {
+          // Keys at or past the pair's last key in the last K/V tile: their V rows hold stale or
+          // poison data and P is 0 there, but 0 * NaN is NaN, so zero them before the PV
+          // product reads them (both groups may do it; they write the same zeros).
+          const int first = it.nk_all - key0;  // 1..128
           if (first < kPrefillTileN) {
-            if (!mbar_wait(bar(SM::bVFull + stage), (gj / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
+            const uint32_t gk = g_item + j;
+            const int stage = gk % NS;
+            if (!mbar_wait(bar(SM::bVFull + stage), (gk / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
             const uint32_t vst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes + SM::kTileBytes;
             const int nchunks = (kPrefillTileN - first) * SM::kHalves * 8;
             for (int i = r; i < nchunks; i += 128) {
@@ -364,25 +417,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             fence_proxy_async_smem();
           }
         }
-        tmem_st32(t_lane + buf * 128, sr);
-        tmem_st32(t_lane + buf * 128 + 32, sr + 32);
+        tmem_st32(t_lane + s_col, sr);
+        tmem_st32(t_lane + s_col + 32, sr + 32);
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds the products of tiles 0..j-1; they have completed, because S of tile j
+          // was issued after them and its commit signalled every earlier MMA done.
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t ov[32];
+            tmem_ld32(t_lane + o_col + ch * 32, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(t_lane + o_col + ch * 32, ov);
+          }
+        }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(SM::bPFull + buf));
+        mbar_arrive(bar(SM::bPFull + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16
-      const uint32_t glast = g + it.n_tiles - 1;
-      if (!mbar_wait(bar(SM::bODone), glast & 1)) { report(a.err, kErrTimeout); break; }
+      if (!mbar_wait(bar(SM::bODone + t), kx & 1)) { report(a.err, kErrTimeout); break; }
       __syncwarp();
       tc_fence_after();
       const float inv = 1.f / l_run;
-      const bool store = r < it.rows;
-      __nv_bfloat16* orow = outg + ((size_t)(it.tok0 + r) * a.Hq + it.head) * D;
+      const bool store = r < it.rows[t];
+      __nv_bfloat16* orow = outg + ((size_t)(it.tok[t] + r) * a.Hq + it.head) * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t ov[32];
-        tmem_ld32(t_lane + 256 + ch * 32, ov);
+        tmem_ld32(t_lane + o_col + ch * 32, ov);
         tc_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -395,10 +460,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
       if (store && a.lse != nullptr)
-        a.lse[(size_t)(it.tok0 + r) * a.Hq + it.head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
       tc_fence_before();
-      mbar_arrive(bar(SM::bOFree));
-      g += it.n_tiles;
+      mbar_arrive(bar(SM::bOFree + t));
+      gx += nt;
+      kx += 1;
     }
   }
 

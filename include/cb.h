@@ -123,8 +123,9 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
  *                 different values agree within rounding; at most CB_MAX_DECODE_CTAS.
  *   phase_events  NULL, or an array of CB_NUM_PHASE_EVENTS cudaEvent_t (created by the
  *                 caller, passed as void*) that the call records on `stream` before the
- *                 planner and after the planner, decode, merge and chunk kernels, so that
- *                 cudaEventElapsedTime gives each kernel's device time.
+ *                 planner and after the planner, the decode kernel, the merge (now part of
+ *                 the decode kernel, so events 2 and 3 are recorded back to back) and the
+ *                 chunk kernel, so that cudaEventElapsedTime gives each kernel's device time.
  */
 #define CB_NUM_PHASE_EVENTS 5
 typedef struct {
