@@ -246,6 +246,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   a.max_blocks = dims->max_blocks_per_seq;
   a.P = dims->num_pages;
   a.KB = gcd_int(block_size, 16);
+  a.KBp = gcd_int(block_size, 128);
   int dctas = options != nullptr ? options->decode_ctas : 0;
   if (dctas <= 0) dctas = ds->sm_count;
   if (dctas > CB_MAX_DECODE_CTAS) dctas = CB_MAX_DECODE_CTAS;
@@ -253,11 +254,13 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   a.prefill_ctas = ds->sm_count;
   a.scale_log2 = scale * 1.4426950408889634f;
 
-  CUtensorMap qmap, kmap, vmap;
+  CUtensorMap qmap, kmap, vmap, kmap_c, vmap_c;
   const uint64_t D = (uint64_t)a.D;
   const uint64_t rows = (uint64_t)a.P * (uint64_t)block_size;
   if ((st = encode_map(&kmap, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
   if ((st = encode_map(&vmap, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
+  if ((st = encode_map(&kmap_c, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KBp)) != CB_OK) return st;
+  if ((st = encode_map(&vmap_c, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KBp)) != CB_OK) return st;
   if ((st = encode_map(&qmap, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 128)) != CB_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -272,7 +275,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
     return cuda_fail(e, "decode launch");
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = mark(3);  // the merge runs inside the decode kernel
-  if (e == cudaSuccess && (e = cb::launch_prefill(a, qmap, kmap, vmap, s)) != cudaSuccess)
+  if (e == cudaSuccess && (e = cb::launch_prefill(a, qmap, kmap_c, vmap_c, s)) != cudaSuccess)
     return cuda_fail(e, "prefill launch");
   if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");

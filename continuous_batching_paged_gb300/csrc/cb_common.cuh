@@ -20,7 +20,6 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 constexpr int kDecodeTileKeys = 16;     // keys per decode pipeline stage
 constexpr int kPrefillTileM = 128;      // queries per prefill tile (TMEM lanes)
-constexpr int kPrefillTileN = 128;      // keys per prefill tile
 constexpr int kMaxDecodeHeadsPerCta = 8;
 
 // Workspace header (int32 words).
@@ -102,6 +101,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test: has the phase of parity `parity` completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase of parity `parity` to complete; false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -163,6 +174,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // with the 128-byte swizzle: the chunk index is XORed with the row index modulo 8.
 __device__ __forceinline__ uint32_t sw128(uint32_t region, uint32_t row, uint32_t chunk) {
   return region + row * 128u + (((chunk ^ row) & 7u) << 4);
+}
+
+// One lane of a fully active warp is elected (the same lane every time); the rest skip.  Used
+// so that a warp runs the tcgen05 issue loop with warp-uniform control flow while a single
+// thread issues the MMAs and the commits that track them.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Register reallocation between warpgroups (all four warps of a warpgroup execute it).  The

@@ -29,7 +29,8 @@ struct AttnArgs {
   char* ws;
   uint32_t* err;
   int S, T, Hq, Hkv, G, D, bs, max_blocks, P;
-  int KB;              // rows per TMA box on the page pool: gcd(bs, 16)
+  int KB;              // rows per TMA box on the page pool, decode pass: gcd(bs, 16)
+  int KBp;             // rows per TMA box on the page pool, chunk pass: gcd(bs, 128)
   int decode_ctas;     // CTAs of the decode pass (<= CB_MAX_DECODE_CTAS)
   int prefill_ctas;    // persistent CTAs of the prefill pass
   float scale_log2;    // softmax scale * log2(e)

@@ -12,13 +12,14 @@
 // warpgroup, which only issues copies and MMAs, to the two softmax warpgroups: 104 + 2 x 200
 // per thread slot = the 3 x 168 the launch provides):
 //   warp 0      TMA producer: Q tiles A and B once per item, then the K and V tiles of 128 keys
-//               gathered page run by page run through the block table into a 2-stage ring
-//               (128-byte swizzle: the layout the tensor-core descriptors read directly).
-//   warp 1      tcgen05 issuer (one thread): for each K/V tile j, S_A = Q_A K_j^T and
-//               S_B = Q_B K_j^T into TMEM; then O_A += P_A V_j and O_B += P_B V_j with P read
-//               from TMEM, interleaved with the next tile's S so the tensor core always has the
-//               other tile's work while one softmax group runs.  Completion is signalled with
-//               tcgen05.commit on mbarriers.  Also owns the TMEM allocation.
+//               gathered page run by page run through the block table (staged in shared memory
+//               once per item) into a 2-stage ring (K and V released separately; 128-byte
+//               swizzle, the layout the tensor-core descriptors read directly).
+//   warp 1      tcgen05 issuer (one elected lane of a converged warp): S_t(j) = Q_t K_j^T into
+//               TMEM, and O_t += P_t(j) V_j with P read from TMEM, then at once S_t(j+1); the
+//               other tile's products keep the tensor core busy while a softmax group runs.
+//               Completion is signalled with tcgen05.commit on mbarriers.  Also owns the TMEM
+//               allocation.
 //   warps 4-7   softmax group A, warps 8-11 softmax group B: thread r owns query row r (TMEM
 //               lane r) of its tile; it loads its 128 scores with tcgen05.ld, applies the causal
 //               mask only on tiles that cross the diagonal, keeps the running max m and sum l in
@@ -31,24 +32,30 @@
 
 namespace cb {
 
+constexpr int kChunkKeys = 128;    // keys per K/V tile of the chunk pass
+constexpr int kEntryCache = 1024;  // block-table entries of an item staged in shared memory
+
 template <int D>
 struct PrefillSmem {
   static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = 128 * 128;             // 128 rows of 128 B
-  static constexpr int kTileBytes = kHalves * kHalfBytes;  // one Q, K or V tile
+  static constexpr int kQHalf = kPrefillTileM * 128;        // 128 query rows of 128 B
+  static constexpr int kQTile = kHalves * kQHalf;
+  static constexpr int kKVHalf = kChunkKeys * 128;          // 128 key rows of 128 B
+  static constexpr int kKVTile = kHalves * kKVHalf;         // one K or V tile
   static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kQ0 = 0;                            // Q_A, then Q_B
-  static constexpr int kStage0 = 2 * kTileBytes;           // stage i: K at +0, V at +kTileBytes
-  static constexpr int kBar = kStage0 + kStages * 2 * kTileBytes;
+  static constexpr int kQ0 = 0;                             // Q_A, then Q_B
+  static constexpr int kStage0 = 2 * kQTile;                // stage i: K at +0, V at +kKVTile
+  static constexpr int kStageBytes = 2 * kKVTile;
+  static constexpr int kBar = kStage0 + kStages * kStageBytes;
   // barrier indices (8 bytes each); [2] arrays are indexed by the tile (A = 0, B = 1)
   static constexpr int bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = bKFull + kStages,
                        bKEmpty = bVFull + kStages, bVEmpty = bKEmpty + kStages,
-                       bSFull = bVEmpty + kStages,
-                       bPFull = bSFull + 2, bODone = bPFull + 2, bOFree = bODone + 2,
-                       bItemFull = bOFree + 2, bItemEmpty = bItemFull + 2,
+                       bSFull = bVEmpty + kStages, bPFull = bSFull + 2, bOFinal = bPFull + 2,
+                       bOFree = bOFinal + 2, bItemFull = bOFree + 2, bItemEmpty = bItemFull + 2,
                        kNumBars = bItemEmpty + 2;
-  static constexpr int kMisc = kBar + kNumBars * 8;        // tmem base, item ids
-  static constexpr int kTotal = kMisc + 64 + 1024;
+  static constexpr int kMisc = kBar + kNumBars * 8;         // tmem base, item ids
+  static constexpr int kEntries = kMisc + 64;               // block-table row of the item
+  static constexpr int kTotal = kEntries + 4 * kEntryCache + 1024;
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -92,8 +99,8 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
   it.rows[1] = it.hasB ? min(kPrefillTileM, q_len - tB * kPrefillTileM) : 0;
   it.nk[0] = it.ctx + tA * kPrefillTileM + it.rows[0];
   it.nk[1] = it.hasB ? it.ctx + tB * kPrefillTileM + it.rows[1] : 0;
-  it.nt[0] = (it.nk[0] + kPrefillTileN - 1) / kPrefillTileN;
-  it.nt[1] = (it.nk[1] + kPrefillTileN - 1) / kPrefillTileN;
+  it.nt[0] = (it.nk[0] + kChunkKeys - 1) / kChunkKeys;
+  it.nt[1] = (it.nk[1] + kChunkKeys - 1) / kChunkKeys;
   it.nk_all = max(it.nk[0], it.nk[1]);
   it.nt_all = max(it.nt[0], it.nt[1]);
   return it;
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SM::bSFull + i), 1);
       mbar_init(bar(SM::bPFull + i), 128);
-      mbar_init(bar(SM::bODone + i), 1);
+      mbar_init(bar(SM::bOFinal + i), 1);
       mbar_init(bar(SM::bOFree + i), 128);
       mbar_init(bar(SM::bItemFull + i), 1);
       mbar_init(bar(SM::bItemEmpty + i), kItemConsumers);
@@ -156,98 +163,108 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   if (warp < 4) {
     regs_dec<kRegsIssue>();
     if (warp == 0) {
-    // ===================================================================== TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
-    const int KB = a.KB;
-    const int nsb = kPrefillTileN / KB;  // page-run boxes per 128-key tile
-    uint32_t g = 0;
-    for (uint32_t k = 0;; ++k) {
-      const int slot = k & 1;
-      int item = -1;
+      // =================================================================== TMA producer
       if (lane == 0) {
-        if (!mbar_wait(bar(SM::bItemEmpty + slot), ((k >> 1) & 1) ^ 1)) report(a.err, kErrTimeout);
-        item = atomicAdd(&hdr->pf_counter, 1);
-        if (item >= n_items) item = -1;
-        item_ids[slot] = item;
-        mbar_arrive(bar(SM::bItemFull + slot));
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
       }
-      item = __shfl_sync(0xffffffffu, item, 0);
-      if (item < 0) break;
-      const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
-      if (lane == 0) {
-        if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
-        mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kTileBytes);
-        for (int t = 0; t < (it.hasB ? 2 : 1); ++t)
-#pragma unroll
-          for (int half = 0; half < SM::kHalves; ++half)
-            tma_load_3d(sbase + SM::kQ0 + t * SM::kTileBytes + half * SM::kHalfBytes, &qmap,
-                        bar(SM::bQFull), half * 64, it.head, it.tok[t]);
-      }
-      const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
-      for (int j = 0; j < it.nt_all; ++j, ++g) {
-        const int stage = g % NS;
-        const uint32_t phase = (g / NS) & 1;
-        const int key0 = j * kPrefillTileN;
-        // Block-table entries of this tile's page runs (loaded before the wait so the load
-        // latency overlaps it).
-        int ent[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int sb = p * 32 + lane;
-          const int pos = key0 + sb * KB;
-          ent[p] = -1;
-          if (sb < nsb && pos < it.nk_all) {
-            const int lb = pos / a.bs;
-            ent[p] = lb < a.max_blocks ? __ldg(row + lb) : -2;
-          }
+      const int KB = a.KBp;
+      const int nsb = kChunkKeys / KB;  // page-run boxes per K/V tile (<= 128)
+      uint32_t g = 0;
+      for (uint32_t k = 0;; ++k) {
+        const int slot = k & 1;
+        int item = -1;
+        if (lane == 0) {
+          if (!mbar_wait(bar(SM::bItemEmpty + slot), ((k >> 1) & 1) ^ 1)) report(a.err, kErrTimeout);
+          item = atomicAdd(&hdr->pf_counter, 1);
+          if (item >= n_items) item = -1;
+          item_ids[slot] = item;
+          mbar_arrive(bar(SM::bItemFull + slot));
         }
-        uint32_t nvalid = 0;
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item < 0) break;
+        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
+        if (lane == 0) {
+          if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
+          mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kQTile);
+          for (int t = 0; t < (it.hasB ? 2 : 1); ++t)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int sb = p * 32 + lane;
-          const bool want = sb < nsb && key0 + sb * KB < it.nk_all;
-          const bool valid = want && ent[p] >= 0 && ent[p] < a.P;
-          if (want && !valid) report(a.err, kErrOutOfRange);
-          nvalid += __popc(__ballot_sync(0xffffffffu, valid));
+            for (int half = 0; half < SM::kHalves; ++half)
+              tma_load_3d(sbase + SM::kQ0 + t * SM::kQTile + half * SM::kQHalf, &qmap,
+                          bar(SM::bQFull), half * 64, it.head, it.tok[t]);
         }
-        const uint32_t bytes = nvalid * (uint32_t)(SM::kHalves * KB * 128);
-        const uint32_t kst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes;
-        const uint32_t vst = kst + SM::kTileBytes;
-        // K and V of a stage are released separately: K once both S products of its tile are
-        // done, V once both PV products are.
-#pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv) {
-          if (lane == 0) {
-            if (!mbar_wait(bar((kv ? SM::bVEmpty : SM::bKEmpty) + stage), phase ^ 1))
-              report(a.err, kErrTimeout);
-            mbar_arrive_expect_tx(bar((kv ? SM::bVFull : SM::bKFull) + stage), bytes);
-          }
-          __syncwarp();
+        const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
+        // Stage the item's block-table entries in shared memory with coalesced loads issued
+        // back to back, so the per-tile loop below never waits on a global load.
+        int* ecache = reinterpret_cast<int*>(smem + SM::kEntries);
+        const int n_ent = min(min((it.nk_all + a.bs - 1) / a.bs, a.max_blocks), kEntryCache);
+        for (int i = lane; i < n_ent; i += 32) ecache[i] = __ldg(row + i);
+        __syncwarp();
+        for (int j = 0; j < it.nt_all; ++j, ++g) {
+          const int stage = g % NS;
+          const uint32_t phase = (g / NS) & 1;
+          const int key0 = j * kChunkKeys;
+          int ent[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int sb = p * 32 + lane;
             const int pos = key0 + sb * KB;
-            if (sb < nsb && pos < it.nk_all && ent[p] >= 0 && ent[p] < a.P) {
-              const int token = ent[p] * a.bs + (pos % a.bs);
+            ent[p] = -1;
+            if (sb < nsb && pos < it.nk_all) {
+              const int lb = pos / a.bs;
+              ent[p] = lb >= a.max_blocks ? -2 : (lb < kEntryCache ? ecache[lb] : __ldg(row + lb));
+            }
+          }
+          uint32_t nvalid = 0;
 #pragma unroll
-              for (int half = 0; half < SM::kHalves; ++half)
-                tma_load_3d((kv ? vst : kst) + half * SM::kHalfBytes + sb * KB * 128,
-                            kv ? &vmap : &kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
-                            half * 64, it.kvh, token);
+          for (int p = 0; p < 4; ++p) {
+            const int sb = p * 32 + lane;
+            const bool want = sb < nsb && key0 + sb * KB < it.nk_all;
+            const bool valid = want && ent[p] >= 0 && ent[p] < a.P;
+            if (want && !valid) report(a.err, kErrOutOfRange);
+            nvalid += __popc(__ballot_sync(0xffffffffu, valid));
+          }
+          const uint32_t bytes = nvalid * (uint32_t)(SM::kHalves * KB * 128);
+          const uint32_t kst = sbase + SM::kStage0 + stage * SM::kStageBytes;
+          const uint32_t vst = kst + SM::kKVTile;
+          // K and V of a stage are released separately: K once both S products of its tile
+          // are done, V once both PV products are.
+#pragma unroll 1
+          for (int kv = 0; kv < 2; ++kv) {
+            if (lane == 0) {
+              if (!mbar_wait(bar((kv ? SM::bVEmpty : SM::bKEmpty) + stage), phase ^ 1))
+                report(a.err, kErrTimeout);
+              mbar_arrive_expect_tx(bar((kv ? SM::bVFull : SM::bKFull) + stage), bytes);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const int sb = p * 32 + lane;
+              const int pos = key0 + sb * KB;
+              if (sb < nsb && pos < it.nk_all && ent[p] >= 0 && ent[p] < a.P) {
+                const int token = ent[p] * a.bs + (pos % a.bs);
+#pragma unroll
+                for (int half = 0; half < SM::kHalves; ++half)
+                  tma_load_3d((kv ? vst : kst) + half * SM::kKVHalf + sb * KB * 128,
+                              kv ? &vmap : &kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
+                              half * 64, it.kvh, token);
+              }
             }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ===================================================================== tcgen05 issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kPrefillTileM, kPrefillTileN, 0);
+    } else if (warp == 1) {
+      // =================================================================== tcgen05 issuer
+      // The whole warp runs this loop (uniform control flow); one elected lane issues each
+      // batch of MMAs together with the commit that tracks it.
+      constexpr uint32_t idesc_s = idesc_bf16(kPrefillTileM, kChunkKeys, 0);
       constexpr uint32_t idesc_o = idesc_bf16(kPrefillTileM, D, 1);
+      // Descriptor of the first 16-wide K slice of each operand region; a slice at byte offset
+      // `off` is the same descriptor with (off >> 4) added to its start-address field.
+      const uint64_t q_desc0 = smem_desc_sw128(sbase + SM::kQ0, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sbase + SM::kStage0, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + SM::kStage0 + SM::kKVTile, SM::kKVHalf, 1024);
       uint32_t g = 0, gx[2] = {0, 0}, kx[2] = {0, 0};
       bool ok = true;
       auto wait = [&](uint32_t b, uint32_t parity) {
@@ -256,63 +273,70 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           ok = false;
         }
       };
-      // Descriptor of the first 16-wide K slice of each operand region; a slice at byte offset
-      // `off` is the same descriptor with (off >> 4) added to its start-address field.
-      const uint64_t q_desc0 = smem_desc_sw128(sbase + SM::kQ0, 16, 1024);
-      const uint64_t kv_desc0 = smem_desc_sw128(sbase + SM::kStage0, 16, 1024);
-      const uint64_t v_desc0 = smem_desc_sw128(sbase + SM::kStage0 + SM::kTileBytes,
-                                               SM::kHalfBytes, 1024);
-      // S_t = Q_t K^T for K/V tile gg into tile t's S buffer.
+      auto commit = [&](uint32_t b) {
+        if (elect_one()) tc_commit(b);
+        __syncwarp();
+      };
+      // S_t = Q_t K^T of K/V tile gg into tile t's S buffer.
       auto issue_s = [&](int t, uint32_t gg) {
         const int stage = gg % NS;
         wait(bar(SM::bKFull + stage), (gg / NS) & 1);
         tc_fence_after();
-        const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kTileBytes) >> 4);
-        const uint64_t kd = kv_desc0 + ((uint32_t)(stage * 2 * SM::kTileBytes) >> 4);
+        const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kQTile) >> 4);
+        const uint64_t kd = k_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * SM::kHalfBytes + (kk & 3) * 32) >> 4;
-          tc_mma_ss(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qo = ((kk >> 2) * SM::kQHalf + (kk & 3) * 32) >> 4;
+            const uint32_t ko = ((kk >> 2) * SM::kKVHalf + (kk & 3) * 32) >> 4;
+            tc_mma_ss(tmem + t * 128, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(SM::bSFull + t));
         }
-        tc_commit(bar(SM::bSFull + t));
+        __syncwarp();
       };
       for (uint32_t k = 0; ok; ++k) {
         const int slot = k & 1;
         wait(bar(SM::bItemFull + slot), (k >> 1) & 1);
         if (!ok) break;
         const int item = item_ids[slot];
-        mbar_arrive(bar(SM::bItemEmpty + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
         if (item < 0) break;
         const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
         const int nt_t[2] = {it.nt[0], it.hasB ? it.nt[1] : 0};
         wait(bar(SM::bQFull), k & 1);
         tc_fence_after();
-        issue_s(0, g);
-        if (nt_t[1] > 0) issue_s(1, g);
-        tc_commit(bar(SM::bKEmpty + g % NS));
+        for (int t = 0; t < 2; ++t)
+          if (nt_t[t] > 0) issue_s(t, g);
+        commit(bar(SM::bKEmpty + g % NS));
         for (int j = 0; j < it.nt_all && ok; ++j) {
           const uint32_t gj = g + j;
           const int stage = gj % NS;
           wait(bar(SM::bVFull + stage), (gj / NS) & 1);
-          const uint64_t vd = v_desc0 + ((uint32_t)(stage * 2 * SM::kTileBytes) >> 4);
+          const uint64_t vd = v_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
 #pragma unroll 1
           for (int t = 0; t < 2; ++t) {
             if (j >= nt_t[t]) continue;
-            wait(bar(SM::bPFull + t), (gx[t] + j) & 1);
+            const uint32_t tt = gx[t] + j;
+            wait(bar(SM::bPFull + t), tt & 1);
             if (j == 0 && kx[t] > 0) wait(bar(SM::bOFree + t), (kx[t] - 1) & 1);
             tc_fence_after();
             const uint32_t p_t = tmem + t * 128;
             const uint32_t o_t = tmem + 256 + t * D;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kPrefillTileN / 16; ++kk)
-              tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-            if (j == nt_t[t] - 1) tc_commit(bar(SM::bODone + t));
+              for (int kk = 0; kk < kChunkKeys / 16; ++kk)
+                tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+              if (j == nt_t[t] - 1) tc_commit(bar(SM::bOFinal + t));
+            }
+            __syncwarp();
             if (j + 1 < nt_t[t]) issue_s(t, gj + 1);
           }
-          tc_commit(bar(SM::bVEmpty + stage));
-          if (j + 1 < it.nt_all) tc_commit(bar(SM::bKEmpty + (gj + 1) % NS));
-          if (j == it.nt_all - 1) tc_commit(bar(SM::bQEmpty));
+          commit(bar(SM::bVEmpty + stage));
+          if (j + 1 < it.nt_all) commit(bar(SM::bKEmpty + (gj + 1) % NS));
+          if (j == it.nt_all - 1) commit(bar(SM::bQEmpty));
         }
         g += it.nt_all;
         for (int t = 0; t < 2; ++t) {
@@ -323,7 +347,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
     }
-    }
   } else {
     regs_inc<kRegsSoftmax>();
     // ===================================================================== softmax groups
@@ -331,7 +354,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int quad = warp & 3;                    // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;               // query row within the tile
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t s_col = t * 128, o_col = 256 + t * D;
+    const uint32_t o_col = 256 + t * D;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
     uint32_t g = 0, gx = 0, kx = 0;
@@ -348,20 +371,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (t == 1 && !it.hasB) continue;
       const int nt = it.nt[t];
       const int diag0 = it.ctx + (it.tok[t] - a.cu_seqlens_q[it.s]);  // row 0's last key
-      const int limit = diag0 + r;                     // row r's last visible key
+      const int limit = diag0 + r;                                     // row r's last key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
-        const uint32_t gj = gx + j;
-        if (!mbar_wait(bar(SM::bSFull + t), gj & 1)) { report(a.err, kErrTimeout); ok = false; break; }
+        const uint32_t tt = gx + j;
+        const uint32_t s_col = t * 128;
+        if (!mbar_wait(bar(SM::bSFull + t), tt & 1)) { report(a.err, kErrTimeout); ok = false; break; }
         __syncwarp();
         tc_fence_after();
         uint32_t sr[128];
 #pragma unroll
         for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + s_col + i * 32, sr + i * 32);
         tc_wait_ld();
-        const int key0 = j * kPrefillTileN;
-        if (key0 + kPrefillTileN - 1 > diag0) {
+        const int key0 = j * kChunkKeys;
+        if (key0 + kChunkKeys - 1 > diag0) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (key0 + c > limit) sr[c] = __float_as_uint(-INFINITY);
@@ -402,16 +426,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           // poison data and P is 0 there, but 0 * NaN is NaN, so zero them before the PV
           // product reads them (both groups may do it; they write the same zeros).
           const int first = it.nk_all - key0;  // 1..128
-          if (first < kPrefillTileN) {
+          if (first < kChunkKeys) {
             const uint32_t gk = g_item + j;
             const int stage = gk % NS;
             if (!mbar_wait(bar(SM::bVFull + stage), (gk / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
-            const uint32_t vst = sbase + SM::kStage0 + stage * 2 * SM::kTileBytes + SM::kTileBytes;
-            const int nchunks = (kPrefillTileN - first) * SM::kHalves * 8;
+            const uint32_t vst = sbase + SM::kStage0 + stage * SM::kStageBytes + SM::kKVTile;
+            const int nchunks = (kChunkKeys - first) * SM::kHalves * 8;
             for (int i = r; i < nchunks; i += 128) {
               const int rr = first + i / (SM::kHalves * 8);
               const int rem = i % (SM::kHalves * 8);
-              const uint32_t addr = sw128(vst + (rem >> 3) * SM::kHalfBytes, rr, rem & 7);
+              const uint32_t addr = sw128(vst + (rem >> 3) * SM::kKVHalf, rr, rem & 7);
               asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
             }
             fence_proxy_async_smem();
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16
-      if (!mbar_wait(bar(SM::bODone + t), kx & 1)) { report(a.err, kErrTimeout); break; }
+      if (!mbar_wait(bar(SM::bOFinal + t), kx & 1)) { report(a.err, kErrTimeout); break; }
       __syncwarp();
       tc_fence_after();
       const float inv = 1.f / l_run;
