@@ -61,36 +61,61 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
 // One warp combines the partial (m, l, o) that CTAs cf..cl wrote for decode sequence `dec`
 // and KV head `kvh` (its G query heads): M = max m_c, w_c = 2^(m_c - M),
 // out = sum_c w_c o_c / sum_c w_c l_c, lse = (M + log2 sum_c w_c l_c) * ln 2.
+// Other CTAs wrote these parts: they are read through L2 (ld.global.cg), never from a stale L1
+// line.  Lane i first fetches (m, l) of part-head pair i, so all of them are read in one round
+// trip; the o loads of a head are then independent of each other.
 template <int D>
 __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* part_ml,
                                             const float* part_o, int dec, int tok, int kvh,
                                             int cf, int cl, int lane) {
   constexpr int PER = D / 32;  // output columns per lane
   __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
-  for (int r = 0; r < a.G; ++r) {
-    const int head = kvh * a.G + r;
-    // Other CTAs wrote these parts: read them through L2 (ld.global.cg), never a stale L1 line.
-    float M = -INFINITY;
-    for (int cc = cf; cc <= cl; ++cc)
-      M = fmaxf(M, __ldcg(part_ml + ((size_t)cc + dec) * a.Hq + head).x);
-    float Lsum = 0.f, acc[PER];
+  const int nparts = cl - cf + 1;
+  for (int r0 = 0; r0 < a.G; r0 += 32 / nparts > 0 ? 32 / nparts : 1) {
+    // lane -> (head r0 + lane / nparts, part lane % nparts)
+    const int rows_here = min(a.G - r0, max(32 / nparts, 1));
+    const int hr = lane / nparts, pc = lane % nparts;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (nparts <= 32 && hr < rows_here)
+      ml = __ldcg(part_ml + ((size_t)(cf + pc) + dec) * a.Hq + kvh * a.G + r0 + hr);
+    for (int rr = 0; rr < rows_here; ++rr) {
+      const int head = kvh * a.G + r0 + rr;
+      float M = -INFINITY;
+      if (nparts <= 32) {
+        for (int cc = 0; cc < nparts; ++cc)
+          M = fmaxf(M, __shfl_sync(0xffffffffu, ml.x, rr * nparts + cc));
+      } else {
+        for (int cc = cf; cc <= cl; ++cc)
+          M = fmaxf(M, __ldcg(part_ml + ((size_t)cc + dec) * a.Hq + head).x);
+      }
+      float Lsum = 0.f, acc[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int cc = cf; cc <= cl; ++cc) {
-      const size_t slot = (size_t)cc + dec;
-      const float2 ml = __ldcg(part_ml + slot * a.Hq + head);
-      const float w = fast_exp2(ml.x - M);
-      Lsum += ml.y * w;
-      const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
+      for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+      for (int cc = 0; cc < nparts; ++cc) {
+        const size_t slot = (size_t)(cf + cc) + dec;
+        float mx, lx;
+        if (nparts <= 32) {
+          mx = __shfl_sync(0xffffffffu, ml.x, rr * nparts + cc);
+          lx = __shfl_sync(0xffffffffu, ml.y, rr * nparts + cc);
+        } else {
+          const float2 v = __ldcg(part_ml + slot * a.Hq + head);
+          mx = v.x;
+          lx = v.y;
+        }
+        const float w = fast_exp2(mx - M);
+        Lsum += lx * w;
+        const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += __ldcg(po + i) * w;
+        for (int i = 0; i < PER; ++i) acc[i] += __ldcg(po + i) * w;
+      }
+      const float inv = 1.f / Lsum;
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
+#pragma unroll
+      for (int i = 0; i < PER / 2; ++i) dst[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      if (lane == 0 && a.lse != nullptr)
+        a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
     }
-    const float inv = 1.f / Lsum;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
-#pragma unroll
-    for (int i = 0; i < PER / 2; ++i) dst[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    if (lane == 0 && a.lse != nullptr)
-      a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
   }
 }
 
@@ -329,12 +354,16 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
       }
       l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
       l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+      // alpha is exactly 1 while the running max stands, which is the common case after the
+      // first tiles: skip the rescale then (warp-uniform test).
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[nt][0] *= al0;
-        o[nt][1] *= al0;
-        o[nt][2] *= al1;
-        o[nt][3] *= al1;
+        for (int nt = 0; nt < NT; ++nt) {
+          o[nt][0] *= al0;
+          o[nt][1] *= al0;
+          o[nt][2] *= al1;
+          o[nt][3] *= al1;
+        }
       }
       uint32_t pa[4];
       pa[0] = pack_bf16x2(p[0][0], p[0][1]);
