@@ -12,10 +12,11 @@
 //   * One producer warp walks the range, prefetches block-table entries 32 at a time, and
 //     issues TMA tensor copies (128-byte swizzle) of each (page run, KV head, 64-wide half of D)
 //     into a multi-stage shared-memory ring guarded by mbarriers.
-//   * One consumer warp per KV head computes S = Q K^T and O += P V for the G query heads of its
-//     group with mma.sync m16n8k16 (bf16 in, fp32 accumulate); the G rows of a GQA group share
-//     every K/V byte read from HBM.  Softmax state lives in registers; row maxima and sums are
-//     reduced with warp shuffles.
+//   * One consumer warp per KV head computes S^T = K Q^T and O^T += V^T P^T for the G query heads
+//     of its group with mma.sync m16n8k16 (bf16 in, fp32 accumulate; keys as the M side, query
+//     heads as N), so the G heads of a GQA group share every K/V byte read from HBM.  It takes
+//     the stage's K and V fragments into registers and releases the stage before computing.
+//     Softmax state lives in registers; maxima and sums are reduced with warp shuffles.
 //
 // Online softmax: for each new tile, m' = max(m, max_j x_j), rescale (l, o) by 2^(m - m'),
 // then add 2^(x_j - m') and 2^(x_j - m') v_j; x_j = scale * log2(e) * q.k_j.
@@ -119,7 +120,245 @@ __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* par
   }
 }
 
-template <int D>
+// Consumer warp of the decode pass: one KV head, its G (<= 8 * NTH) query heads, every tile of
+// the CTA's range.  Products are taken with keys as the m16n8k16 M side and query heads as N:
+//   S^T (16 keys x 8 heads)  = K (16 keys x 16 d) . Q^T (16 d x 8 heads), over D/16 k-steps;
+//   O^T (16 d x 8 heads)    += V^T (16 d x 16 keys) . P^T (16 keys x 8 heads), over D/16 m-tiles.
+// P^T is moved from the S^T accumulator layout to the B-operand layout with movmatrix.  With
+// NTH == 1 the warp first loads every K and V fragment of the stage into registers and releases
+// the stage before computing, so the producer refills it sooner.
+template <int D, int NTH>
+__device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase, uint32_t bar_full,
+                                               uint32_t bar_empty, const StageInfo* info, int c,
+                                               int hg, int h, long long n_my, long long ntiles,
+                                               int N, const WsLayout& L, int lane) {
+  using SM = DecodeSmem<D>;
+  constexpr int KS = D / 16;  // k-steps of S^T over the head dim
+  constexpr int MT = D / 16;  // m-tiles of O^T over the head dim
+  constexpr bool kPreload = (NTH == 1);
+  const int kvh = hg * kMaxDecodeHeadsPerCta + h;  // global KV head
+  const int g = lane >> 2, tq = lane & 3;          // mma fragment coordinates
+  float2* part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml);
+  float* part_o = reinterpret_cast<float*>(a.ws + L.part_o);
+  int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
+  const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
+  __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
+  const float sl2 = a.scale_log2;
+
+  uint32_t qb[NTH][KS][2];
+  float o[MT][NTH][4];
+  float mrun[NTH][2], lrun[NTH][2];
+  const int rowbase = h * kDecodeTileKeys;
+  // ldmatrix lane -> (key, 16-byte chunk) of the K (non-transposed) and V (transposed) loads
+  const int k_key = (lane & 7) + (((lane >> 3) & 1) << 3), k_csel = lane >> 4;
+  const int v_key = (lane & 7) + ((lane >> 4) << 3), v_csel = (lane >> 3) & 1;
+
+  for (long long it = 0; it < n_my; ++it) {
+    const int stage = (int)(it % kDecodeStages);
+    const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+    if (!mbar_wait(bar_full + 8 * stage, phase)) {
+      report(a.err, kErrTimeout);
+      break;
+    }
+    const StageInfo si = info[stage];
+    if (si.flags & kInfoFirst) {
+#pragma unroll
+      for (int ht = 0; ht < NTH; ++ht) {
+        mrun[ht][0] = mrun[ht][1] = -INFINITY;
+        lrun[ht][0] = lrun[ht][1] = 0.f;
+        const int hl = ht * 8 + g;  // query head within the group held as column g of Q^T
+        const uint32_t* qrow = q32 + (((size_t)si.tok * a.Hq + kvh * a.G + hl) * D) / 2;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qb[ht][ks][0] = hl < a.G ? __ldg(qrow + ks * 8 + tq) : 0u;
+          qb[ht][ks][1] = hl < a.G ? __ldg(qrow + ks * 8 + 4 + tq) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) o[mt][ht][0] = o[mt][ht][1] = o[mt][ht][2] = o[mt][ht][3] = 0.f;
+      }
+    }
+    const uint32_t kst = sbase + stage * SM::kStageBytes;
+    const uint32_t vst = kst + SM::kKVBytes;
+    const bool tail = si.key0 + kDecodeTileKeys > si.kv;
+
+    // ---- K fragments (A operand of S^T: rows = keys, k = head dim)
+    uint32_t kf[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int chunk = 2 * ks + k_csel;
+      ldsm_x4(sw128(kst + (chunk >> 3) * SM::kHalfBytes, rowbase + k_key, chunk & 7), kf[ks][0],
+              kf[ks][1], kf[ks][2], kf[ks][3]);
+    }
+    // ---- keys past kv_len: their V rows may hold stale or poison data; P is 0 there, but
+    // 0 * NaN is NaN, so zero those rows of this head before they are read.
+    if (tail) {
+      const int first = si.kv - si.key0;  // 1..15
+      const int nrow = kDecodeTileKeys - first;
+      for (int i = lane; i < nrow * SM::kHalves * 8; i += 32) {
+        const int r = first + i / (SM::kHalves * 8);
+        const int rem = i % (SM::kHalves * 8);
+        const uint32_t addr = sw128(vst + (rem >> 3) * SM::kHalfBytes, rowbase + r, rem & 7);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+      }
+      __syncwarp();
+    }
+    // ---- V fragments (A operand of O^T: rows = head dim, k = keys), loaded transposed
+    uint32_t vf[kPreload ? MT : 1][4];
+    if constexpr (kPreload) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int chunk = 2 * mt + v_csel;
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, rowbase + v_key, chunk & 7),
+                  vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+      }
+      if (tail) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+    }
+
+    // ---- S^T = K Q^T
+    float s[NTH][4];
+#pragma unroll
+    for (int ht = 0; ht < NTH; ++ht) {
+      s[ht][0] = s[ht][1] = s[ht][2] = s[ht][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) mma_bf16_16816(s[ht], kf[ks], qb[ht][ks][0], qb[ht][ks][1]);
+    }
+    if (tail) {
+      const bool dead0 = si.key0 + g >= si.kv, dead1 = si.key0 + g + 8 >= si.kv;
+#pragma unroll
+      for (int ht = 0; ht < NTH; ++ht) {
+        if (dead0) s[ht][0] = s[ht][1] = -INFINITY;
+        if (dead1) s[ht][2] = s[ht][3] = -INFINITY;
+      }
+    }
+    // ---- online softmax per query head (columns 2 tq and 2 tq + 1), reduced over the 16 keys
+    uint32_t pb[NTH][2];
+    bool resc = false;
+    float al[NTH][2];
+#pragma unroll
+    for (int ht = 0; ht < NTH; ++ht) {
+      float ma = fmaxf(s[ht][0], s[ht][2]), mb = fmaxf(s[ht][1], s[ht][3]);
+#pragma unroll
+      for (int x = 4; x < 32; x <<= 1) {
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, x));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, x));
+      }
+      const float na = fmaxf(mrun[ht][0], ma * sl2), nb = fmaxf(mrun[ht][1], mb * sl2);
+      al[ht][0] = fast_exp2(mrun[ht][0] - na);
+      al[ht][1] = fast_exp2(mrun[ht][1] - nb);
+      mrun[ht][0] = na;
+      mrun[ht][1] = nb;
+      const float p0 = fast_exp2(fmaf(s[ht][0], sl2, -na)), p1 = fast_exp2(fmaf(s[ht][1], sl2, -nb));
+      const float p2 = fast_exp2(fmaf(s[ht][2], sl2, -na)), p3 = fast_exp2(fmaf(s[ht][3], sl2, -nb));
+      lrun[ht][0] = lrun[ht][0] * al[ht][0] + (p0 + p2);
+      lrun[ht][1] = lrun[ht][1] * al[ht][1] + (p1 + p3);
+      resc |= (al[ht][0] != 1.f) || (al[ht][1] != 1.f);
+      pb[ht][0] = movm_trans(pack_bf16x2(p0, p1));  // keys 0-7:  B[k = 2tq, 2tq+1][n = g]
+      pb[ht][1] = movm_trans(pack_bf16x2(p2, p3));  // keys 8-15
+    }
+    // alpha is exactly 1 while the running max stands (the common case): skip the rescale then
+    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int ht = 0; ht < NTH; ++ht) {
+          o[mt][ht][0] *= al[ht][0];
+          o[mt][ht][1] *= al[ht][1];
+          o[mt][ht][2] *= al[ht][0];
+          o[mt][ht][3] *= al[ht][1];
+        }
+    }
+    // ---- O^T += V^T P^T
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t va[4];
+      if constexpr (kPreload) {
+        va[0] = vf[mt][0];
+        va[1] = vf[mt][1];
+        va[2] = vf[mt][2];
+        va[3] = vf[mt][3];
+      } else {
+        const int chunk = 2 * mt + v_csel;
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, rowbase + v_key, chunk & 7), va[0],
+                  va[1], va[2], va[3]);
+      }
+#pragma unroll
+      for (int ht = 0; ht < NTH; ++ht) mma_bf16_16816(o[mt][ht], va, pb[ht][0], pb[ht][1]);
+    }
+    if constexpr (!kPreload) {
+      if (tail) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+    }
+
+    if (si.flags & kInfoLast) {
+#pragma unroll
+      for (int ht = 0; ht < NTH; ++ht) {
+        float la = lrun[ht][0], lb = lrun[ht][1];
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+          la += __shfl_xor_sync(0xffffffffu, la, x);
+          lb += __shfl_xor_sync(0xffffffffu, lb, x);
+        }
+        const int ha = ht * 8 + 2 * tq, hb = ha + 1;  // query heads (within the group) of my columns
+        if (si.flags & kInfoComplete) {
+          const float ia = 1.f / la, ib = 1.f / lb;
+          const int hrow = ht * 8 + g;  // after the transpose a thread holds query head g
+          uint32_t* orow = reinterpret_cast<uint32_t*>(
+              outg + ((size_t)si.tok * a.Hq + kvh * a.G + hrow) * D);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t lo = movm_trans(pack_bf16x2(o[mt][ht][0] * ia, o[mt][ht][1] * ib));
+            const uint32_t hi = movm_trans(pack_bf16x2(o[mt][ht][2] * ia, o[mt][ht][3] * ib));
+            if (hrow < a.G) {
+              orow[(16 * mt + 2 * tq) / 2] = lo;
+              orow[(16 * mt + 8 + 2 * tq) / 2] = hi;
+            }
+          }
+          if (a.lse != nullptr && g == 0) {
+            if (ha < a.G) a.lse[(size_t)si.tok * a.Hq + kvh * a.G + ha] = (mrun[ht][0] + __log2f(la)) * 0.6931471805599453f;
+            if (hb < a.G) a.lse[(size_t)si.tok * a.Hq + kvh * a.G + hb] = (mrun[ht][1] + __log2f(lb)) * 0.6931471805599453f;
+          }
+        } else {
+          const size_t slot = (size_t)c + si.dec;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            if (ha < a.G) {
+              float* po = part_o + (slot * a.Hq + kvh * a.G + ha) * D + 16 * mt + g;
+              po[0] = o[mt][ht][0];
+              po[8] = o[mt][ht][2];
+            }
+            if (hb < a.G) {
+              float* po = part_o + (slot * a.Hq + kvh * a.G + hb) * D + 16 * mt + g;
+              po[0] = o[mt][ht][1];
+              po[8] = o[mt][ht][3];
+            }
+          }
+          if (g == 0) {
+            if (ha < a.G) part_ml[slot * a.Hq + kvh * a.G + ha] = make_float2(mrun[ht][0], la);
+            if (hb < a.G) part_ml[slot * a.Hq + kvh * a.G + hb] = make_float2(mrun[ht][1], lb);
+          }
+        }
+      }
+      if (!(si.flags & kInfoComplete)) {
+        // Split sequence: the last warp to finish this (sequence, KV head) merges all parts.
+        const int cf = cta_of_tile(si.p0, ntiles, N), cl = cta_of_tile(si.p1 - 1, ntiles, N);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == cl - cf;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, lane);
+        }
+      }
+    }
+  }
+}
+
+template <int D, int NTH>
 __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
     decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
@@ -255,201 +494,8 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
       ++d;
     }
   } else if (warp < HB) {
-    // ===================================================================== consumer warps
-    const int h = warp;                                    // KV head within this CTA
-    const int kvh = hg * kMaxDecodeHeadsPerCta + h;        // global KV head
-    const int g = lane >> 2, tq = lane & 3;                // mma fragment coordinates
-    const float2* dummy = nullptr;
-    (void)dummy;
-    float2* part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml);
-    float* part_o = reinterpret_cast<float*>(a.ws + L.part_o);
-    int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-    __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
-
-    constexpr int KS = D / 16;   // k-steps over the head dimension
-    constexpr int NT = D / 8;    // n-tiles of the output
-    uint32_t qa[KS][4];
-    float o[NT][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const long long n_my = t1 - t0;
-    for (long long it = 0; it < n_my; ++it) {
-      const int stage = (int)(it % kDecodeStages);
-      const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
-      if (!mbar_wait(bar_full + 8 * stage, phase)) {
-        report(a.err, kErrTimeout);
-        break;
-      }
-      const StageInfo si = info[stage];
-      if (si.flags & kInfoFirst) {
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-        // Query fragments (rows = the G query heads of this KV head; rows >= G are zero).
-        const int r0 = g, r1 = g + 8;
-        const bool v0 = r0 < a.G, v1 = r1 < a.G;
-        const uint32_t* q0 =
-            reinterpret_cast<const uint32_t*>(qg + ((size_t)si.tok * a.Hq + kvh * a.G + r0) * D);
-        const uint32_t* q1 =
-            reinterpret_cast<const uint32_t*>(qg + ((size_t)si.tok * a.Hq + kvh * a.G + r1) * D);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int w = (ks * 16 + 2 * tq) / 2;
-          qa[ks][0] = v0 ? __ldg(q0 + w) : 0u;
-          qa[ks][1] = v1 ? __ldg(q1 + w) : 0u;
-          qa[ks][2] = v0 ? __ldg(q0 + w + 4) : 0u;
-          qa[ks][3] = v1 ? __ldg(q1 + w + 4) : 0u;
-        }
-      }
-      const uint32_t kst = sbase + stage * SM::kStageBytes;
-      const uint32_t vst = kst + SM::kKVBytes;
-      const int rowbase = h * kDecodeTileKeys;
-
-      // ---- S = Q K^T over this tile's 16 keys (two n-tiles of 8 keys)
-      float s[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-      {
-        const int kk = (lane & 7) + ((lane >> 4) << 3);
-        const int csel = (lane >> 3) & 1;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int half = ks >> 2;
-          const int chunk = ((ks & 3) << 1) + csel;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(sw128(kst + half * SM::kHalfBytes, rowbase + kk, chunk), b0, b1, b2, b3);
-          mma_bf16_16816(s[0], qa[ks], b0, b1);
-          mma_bf16_16816(s[1], qa[ks], b2, b3);
-        }
-      }
-      const bool tail = si.key0 + kDecodeTileKeys > si.kv;
-      if (tail) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int key = si.key0 + nt * 8 + 2 * tq + (j & 1);
-            if (key >= si.kv) s[nt][j] = -INFINITY;
-          }
-      }
-      // ---- online softmax (rows g and g + 8)
-      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])) * a.scale_log2;
-      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])) * a.scale_log2;
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float p[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = fast_exp2(fmaf(s[nt][0], a.scale_log2, -mn0));
-        p[nt][1] = fast_exp2(fmaf(s[nt][1], a.scale_log2, -mn0));
-        p[nt][2] = fast_exp2(fmaf(s[nt][2], a.scale_log2, -mn1));
-        p[nt][3] = fast_exp2(fmaf(s[nt][3], a.scale_log2, -mn1));
-      }
-      l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-      l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-      // alpha is exactly 1 while the running max stands, which is the common case after the
-      // first tiles: skip the rescale then (warp-uniform test).
-      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[nt][0] *= al0;
-          o[nt][1] *= al0;
-          o[nt][2] *= al1;
-          o[nt][3] *= al1;
-        }
-      }
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-
-      // ---- keys past kv_len: their V rows may hold stale or poison data; P is 0 there, but
-      // 0 * NaN is NaN, so zero those rows of this head before they enter the product.
-      if (tail) {
-        const int first = si.kv - si.key0;  // 1..15
-        const int nrow = kDecodeTileKeys - first;
-        for (int i = lane; i < nrow * SM::kHalves * 8; i += 32) {
-          const int r = first + i / (SM::kHalves * 8);
-          const int rem = i % (SM::kHalves * 8);
-          const int half = rem >> 3, ch = rem & 7;
-          const uint32_t addr = sw128(vst + half * SM::kHalfBytes, rowbase + r, ch);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
-        }
-        __syncwarp();
-      }
-      // ---- O += P V
-      {
-        const int kk = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int csel = lane >> 4;
-#pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          const int cidx = 2 * np + csel;
-          const int half = cidx >> 3;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sw128(vst + half * SM::kHalfBytes, rowbase + kk, cidx & 7), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * np], pa, b0, b1);
-          mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
-        }
-      }
-      if (tail) fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
-
-      if (si.flags & kInfoLast) {
-        float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-        lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
-        float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-        lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-        const int rows[2] = {g, g + 8};
-        const float ls[2] = {lt0, lt1};
-        const float ms[2] = {m0, m1};
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          if (rows[hr] >= a.G) continue;
-          const int head = kvh * a.G + rows[hr];
-          if (si.flags & kInfoComplete) {
-            const float inv = 1.f / ls[hr];
-            uint32_t* dst =
-                reinterpret_cast<uint32_t*>(outg + ((size_t)si.tok * a.Hq + head) * D);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              dst[(nt * 8 + 2 * tq) / 2] =
-                  pack_bf16x2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
-            if (a.lse != nullptr && tq == 0)
-              a.lse[(size_t)si.tok * a.Hq + head] = (ms[hr] + __log2f(ls[hr])) * 0.6931471805599453f;
-          } else {
-            const size_t slot = (size_t)c + si.dec;
-            float* po = part_o + (slot * a.Hq + head) * D;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              *reinterpret_cast<float2*>(po + nt * 8 + 2 * tq) =
-                  make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
-            if (tq == 0) part_ml[slot * a.Hq + head] = make_float2(ms[hr], ls[hr]);
-          }
-        }
-        if (!(si.flags & kInfoComplete)) {
-          // Split sequence: the last warp to finish this (sequence, KV head) merges all parts.
-          const int cf = cta_of_tile(si.p0, ntiles, N), cl = cta_of_tile(si.p1 - 1, ntiles, N);
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == cl - cf;
-          last = __shfl_sync(0xffffffffu, last, 0);
-          if (last) {
-            __threadfence();
-            merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, lane);
-          }
-        }
-      }
-    }
+    decode_consume<D, NTH>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
+                           L, lane);
   }
 }
 
@@ -461,14 +507,20 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, 1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SM::kTotal);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
   dim3 grid(a.decode_ctas, (a.Hkv + kMaxDecodeHeadsPerCta - 1) / kMaxDecodeHeadsPerCta);
-  decode_kernel<D><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
+  if (a.G <= 8)
+    decode_kernel<D, 1><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
+  else
+    decode_kernel<D, 2><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 
