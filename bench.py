@@ -57,6 +57,8 @@ def parse_args():
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed")
     p.add_argument("--decode-ctas", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--serial", action="store_true",
+                   help="run the chunk kernel after the decode kernel instead of concurrently")
     return p.parse_args()
 
 
@@ -367,17 +369,22 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(cb.NUM_PHASE_EVENTS + 1)]
-    for e in ev:
+    # ev_start / ev_end bracket the step on the launching stream; the library records its five
+    # phase events around the planner, the decode kernel and the chunk kernel (cb_options).
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ph = [torch.cuda.Event(enable_timing=True) for _ in range(cb.NUM_PHASE_EVENTS)]
+    for e in [ev_start, ev_end] + ph:
         e.record()
 
     def step(record):
         if record:
-            ev[0].record()
+            ev_start.record()
         cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
         cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, out=out,
                                   workspace=ws, decode_ctas=args.decode_ctas,
-                                  phase_events=ev[1:] if record else None)
+                                  phase_events=ph if record else None, serial=args.serial)
+        if record:
+            ev_end.record()
 
     # correctness guard before timing: the error word must be clear after one step
     step(False)
@@ -398,8 +405,9 @@ def main():
         if soak % 50 == 0:
             torch.cuda.synchronize()
 
-    names = ["append"] + list(cb.PHASES)
-    acc = {n: 0.0 for n in names}
+    spans = {"append": (ev_start, ph[0]), "plan": (ph[0], ph[1]), "decode": (ph[1], ph[2]),
+             "chunk": (ph[3], ph[4])}
+    acc = {n: 0.0 for n in spans}
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -407,11 +415,10 @@ def main():
     for _ in range(args.steps):
         flush.fill_(1.0)
         step(True)
-        ev[-1].synchronize()
-        d = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
-        for n, x in zip(names, d):
-            acc[n] += x
-        step_ms += ev[0].elapsed_time(ev[-1])
+        ev_end.synchronize()
+        for n, (e0_, e1_) in spans.items():
+            acc[n] += e0_.elapsed_time(e1_)
+        step_ms += ev_start.elapsed_time(ev_end)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
@@ -420,7 +427,7 @@ def main():
 
     ms = dist_max(step_ms / args.steps, world, dev)
     value = world * b.num_tokens / (ms / 1000.0)
-    per_kernel = {n: acc[n] / args.steps for n in names}
+    per_kernel = {n: acc[n] / args.steps for n in spans}
 
     # e2e: the step through the public API with inputs from pinned host memory, output back.
     h_q = torch.from_numpy(b.q.view(np.int16)).pin_memory()
@@ -489,6 +496,7 @@ def main():
         "e2e": {"value": world * b.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 4 * args.steps,  # append, plan, decode (with merge), chunk
+        "concurrent_decode_chunk": not args.serial,
         "roofline": roof,
         "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
                    "gbs": dec_gbs, "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,

@@ -36,6 +36,10 @@ struct DeviceState {
   bool ready = false;
   int sm_count = 0;
   uint32_t* err = nullptr;
+  cudaStream_t aux = nullptr;      // second stream for the chunk kernel (created once)
+  cudaEvent_t ev_fork = nullptr;   // timing-free fork / join events (created once)
+  cudaEvent_t ev_join = nullptr;
+  std::mutex launch_mu;            // one fork/join sequence at a time per device
 };
 
 constexpr int kMaxDevices = 64;
@@ -63,6 +67,10 @@ cb_status device_state(DeviceState** out) {
     e = cudaGetSymbolAddress(&p, g_cb_error_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     st.err = static_cast<uint32_t*>(p);
+    e = cudaStreamCreateWithFlags(&st.aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "creating the library's stream and events");
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -265,20 +273,34 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* const* ev = options != nullptr ? options->phase_events : nullptr;
-  auto mark = [&](int i) -> cudaError_t {
-    return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
+  const bool serial = options != nullptr && (options->flags & CB_OPT_SERIAL);
+  auto mark = [&](int i, cudaStream_t on) -> cudaError_t {
+    return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), on) : cudaSuccess;
   };
-  cudaError_t e = mark(0);
+  std::lock_guard<std::mutex> lk(ds->launch_mu);
+  cudaError_t e = mark(0, s);
   if (e == cudaSuccess && (e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
-  if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && (e = cb::launch_decode(a, kmap, vmap, s)) != cudaSuccess)
-    return cuda_fail(e, "decode launch");
-  if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = mark(3);  // the merge runs inside the decode kernel
-  if (e == cudaSuccess && (e = cb::launch_prefill(a, qmap, kmap_c, vmap_c, s)) != cudaSuccess)
-    return cuda_fail(e, "prefill launch");
-  if (e == cudaSuccess) e = mark(4);
+  if (e == cudaSuccess) e = mark(1, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  cudaStream_t cs = serial ? s : ds->aux;
+  if (!serial) {
+    // fork: the chunk kernel's stream waits for the planner
+    if ((e = cudaEventRecord(ds->ev_fork, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ds->aux, ds->ev_fork, 0)) != cudaSuccess)
+      return cuda_fail(e, "fork to the chunk stream");
+  }
+  if ((e = cb::launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  if ((e = mark(3, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  if ((e = cb::launch_prefill(a, qmap, kmap_c, vmap_c, cs)) != cudaSuccess)
+    return cuda_fail(e, "prefill launch");
+  if ((e = mark(4, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  if (!serial) {
+    // join: work queued on the caller's stream after this call waits for the chunk kernel
+    if ((e = cudaEventRecord(ds->ev_join, ds->aux)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, ds->ev_join, 0)) != cudaSuccess)
+      return cuda_fail(e, "join from the chunk stream");
+  }
   return CB_OK;
 }
 

@@ -121,16 +121,24 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
  *   decode_ctas   number of CTAs the decode pass spreads its key tiles over (0 = one per SM;
  *                 1 forces every decode sequence into a single unsplit pass).  Results for
  *                 different values agree within rounding; at most CB_MAX_DECODE_CTAS.
+ *   flags         CB_OPT_SERIAL: run the chunk kernel after the decode kernel on `stream`
+ *                 instead of concurrently on the library's second stream.
  *   phase_events  NULL, or an array of CB_NUM_PHASE_EVENTS cudaEvent_t (created by the
- *                 caller, passed as void*) that the call records on `stream` before the
- *                 planner and after the planner, the decode kernel, the merge (now part of
- *                 the decode kernel, so events 2 and 3 are recorded back to back) and the
- *                 chunk kernel, so that cudaEventElapsedTime gives each kernel's device time.
+ *                 caller, passed as void*).  The call records [0] on `stream` before the
+ *                 planner, [1] after it, [2] after the decode kernel (which also merges split
+ *                 sequences), and [3] / [4] just before / after the chunk kernel on the stream
+ *                 that runs it, so cudaEventElapsedTime gives each kernel's device time.
+ *
+ * Concurrency: by default the decode kernel (HBM-bound) runs on `stream` while the chunk kernel
+ * (tensor-bound) runs on a second stream that the library creates once per device, forked from
+ * and joined back into `stream` with events; the chunk kernel's CTAs take SMs as decode CTAs
+ * finish.  Work the caller queues on `stream` after the call waits for both.
  */
 #define CB_NUM_PHASE_EVENTS 5
+#define CB_OPT_SERIAL 1
 typedef struct {
   int32_t decode_ctas;
-  int32_t reserved0;
+  int32_t flags;
   void* const* phase_events;
   int64_t reserved[4];
 } cb_options;
