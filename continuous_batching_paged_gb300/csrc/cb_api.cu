@@ -119,11 +119,12 @@ cb_status check_dims(const cb_dims* d, int32_t block_size) {
   return CB_OK;
 }
 
+// 3-D bf16 tensor map with 128-byte swizzle and a box of 64 x box1 x box2 elements.
 cb_status encode_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t box_rows) {
+                     uint64_t s1_bytes, uint64_t s2_bytes, uint32_t box1, uint32_t box2) {
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
-  const cuuint32_t box[3] = {64, 1, box_rows};
+  const cuuint32_t box[3] = {64, box1, box2};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -265,11 +266,14 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   CUtensorMap qmap, kmap, vmap, kmap_c, vmap_c;
   const uint64_t D = (uint64_t)a.D;
   const uint64_t rows = (uint64_t)a.P * (uint64_t)block_size;
-  if ((st = encode_map(&kmap, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
-  if ((st = encode_map(&vmap, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KB)) != CB_OK) return st;
-  if ((st = encode_map(&kmap_c, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KBp)) != CB_OK) return st;
-  if ((st = encode_map(&vmap_c, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, a.KBp)) != CB_OK) return st;
-  if ((st = encode_map(&qmap, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 128)) != CB_OK) return st;
+  // Decode pass: dims (d, token, head) so one box {64, KB tokens, up to 8 heads} lands in shared
+  // memory as [head][token] rows; chunk pass: dims (d, head, token), box {64, 1 head, KBp tokens}.
+  const uint32_t HB = (uint32_t)(Hkv < cb::kMaxDecodeHeadsPerCta ? Hkv : cb::kMaxDecodeHeadsPerCta);
+  if ((st = encode_map(&kmap, k_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
+  if ((st = encode_map(&vmap, v_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
+  if ((st = encode_map(&kmap_c, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
+  if ((st = encode_map(&vmap_c, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
+  if ((st = encode_map(&qmap, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 1, 128)) != CB_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* const* ev = options != nullptr ? options->phase_events : nullptr;

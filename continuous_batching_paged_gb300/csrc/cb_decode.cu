@@ -148,10 +148,13 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
   uint32_t qb[NTH][KS][2];
   float o[MT][NTH][4];
   float mrun[NTH][2], lrun[NTH][2];
-  const int rowbase = h * kDecodeTileKeys;
+  // Stage layout of one 64-wide half of K (or V): runs of KB keys, each run [HB heads][KB keys]
+  // of 128-byte rows, so key k of this warp's head is row (k / KB) * HB * KB + h * KB + k % KB.
+  const int KB = a.KB, HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
+  auto row_of = [&](int k) { return (k / KB) * HB * KB + h * KB + (k % KB); };
   // ldmatrix lane -> (key, 16-byte chunk) of the K (non-transposed) and V (transposed) loads
-  const int k_key = (lane & 7) + (((lane >> 3) & 1) << 3), k_csel = lane >> 4;
-  const int v_key = (lane & 7) + ((lane >> 4) << 3), v_csel = (lane >> 3) & 1;
+  const int k_row = row_of((lane & 7) + (((lane >> 3) & 1) << 3)), k_csel = lane >> 4;
+  const int v_row = row_of((lane & 7) + ((lane >> 4) << 3)), v_csel = (lane >> 3) & 1;
 
   for (long long it = 0; it < n_my; ++it) {
     const int stage = (int)(it % kDecodeStages);
@@ -186,7 +189,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int chunk = 2 * ks + k_csel;
-      ldsm_x4(sw128(kst + (chunk >> 3) * SM::kHalfBytes, rowbase + k_key, chunk & 7), kf[ks][0],
+      ldsm_x4(sw128(kst + (chunk >> 3) * SM::kHalfBytes, k_row, chunk & 7), kf[ks][0],
               kf[ks][1], kf[ks][2], kf[ks][3]);
     }
     // ---- keys past kv_len: their V rows may hold stale or poison data; P is 0 there, but
@@ -197,7 +200,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
       for (int i = lane; i < nrow * SM::kHalves * 8; i += 32) {
         const int r = first + i / (SM::kHalves * 8);
         const int rem = i % (SM::kHalves * 8);
-        const uint32_t addr = sw128(vst + (rem >> 3) * SM::kHalfBytes, rowbase + r, rem & 7);
+        const uint32_t addr = sw128(vst + (rem >> 3) * SM::kHalfBytes, row_of(r), rem & 7);
         asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
       }
       __syncwarp();
@@ -208,7 +211,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int chunk = 2 * mt + v_csel;
-        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, rowbase + v_key, chunk & 7),
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, v_row, chunk & 7),
                   vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
       }
       if (tail) fence_proxy_async_smem();
@@ -280,7 +283,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
         va[3] = vf[mt][3];
       } else {
         const int chunk = 2 * mt + v_csel;
-        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, rowbase + v_key, chunk & 7), va[0],
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * SM::kHalfBytes, v_row, chunk & 7), va[0],
                   va[1], va[2], va[3]);
       }
 #pragma unroll
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
       tma_prefetch_desc(&vmap);
     }
     const int KB = a.KB;
-    const int nsb = kDecodeTileKeys / KB;        // TMA boxes per head per tile
+    const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
     const int tiles_per_batch = 32 / nsb;
     int d = cta_first[c];
     long long t = t0;
@@ -441,18 +444,14 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
           abort = __shfl_sync(0xffffffffu, abort, 0);
           if (abort) break;
           const int key0 = (int)(tile - p0) * kDecodeTileKeys;
-          // (sub-box sb, head h) pairs of this tile, 32 per pass over the warp.
-          const int npairs = nsb * HB;
-          uint32_t nvalid = 0;
-          for (int base = 0; base < npairs; base += 32) {
-            const int pr = base + lane, sb = pr / HB;
-            const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (sb < nsb ? sb : 0));
-            const int pos = key0 + sb * KB;
-            const bool want = pr < npairs && pos < kv;
-            const bool valid = want && e >= 0 && e < a.P;
-            if (want && !valid) report(a.err, kErrOutOfRange);
-            nvalid += __popc(__ballot_sync(0xffffffffu, valid));
-          }
+          // One TMA box per (page run sb, half of D, K or V) covers all HB heads of the run:
+          // lane sb handles run sb (nsb <= 16 runs per tile).
+          const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (lane < nsb ? lane : 0));
+          const int pos = key0 + lane * KB;
+          const bool want = lane < nsb && pos < kv;
+          const bool valid = want && e >= 0 && e < a.P;
+          if (want && !valid) report(a.err, kErrOutOfRange);
+          const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
           if (lane == 0) {
             StageInfo& si = info[stage];
             si.seq = s;
@@ -465,27 +464,20 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             si.flags = (tile == lo ? kInfoFirst : 0u) | (tile == hi - 1 ? kInfoLast : 0u) |
                        (complete ? kInfoComplete : 0u);
             mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                  nvalid * (uint32_t)(2 * SM::kHalves * KB * 128));
+                                  nvalid * (uint32_t)(2 * SM::kHalves * KB * HB * 128));
           }
           __syncwarp();
-          for (int base = 0; base < npairs; base += 32) {
-            const int pr = base + lane, sb = pr / HB, h = pr % HB;
-            const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (sb < nsb ? sb : 0));
-            const int pos = key0 + sb * KB;
-            const bool valid = pr < npairs && pos < kv && e >= 0 && e < a.P;
-            if (valid) {
-              const int token = e * a.bs + (pos % a.bs);
-              const int head = hg * kMaxDecodeHeadsPerCta + h;
-              const uint32_t kst = sbase + stage * SM::kStageBytes;
-              const uint32_t vst = kst + SM::kKVBytes;
-              const uint32_t off = (uint32_t)(h * kDecodeTileKeys * 128 + sb * KB * 128);
+          if (valid) {
+            const int token = e * a.bs + (pos % a.bs);
+            const uint32_t kst = sbase + stage * SM::kStageBytes;
+            const uint32_t vst = kst + SM::kKVBytes;
+            const uint32_t off = (uint32_t)(lane * HB * KB * 128);  // run sb: [HB heads][KB keys]
 #pragma unroll
-              for (int half = 0; half < SM::kHalves; ++half) {
-                tma_load_3d(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
-                            half * 64, head, token);
-                tma_load_3d(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
-                            half * 64, head, token);
-              }
+            for (int half = 0; half < SM::kHalves; ++half) {
+              tma_load_3d(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
+                          half * 64, token, hg * kMaxDecodeHeadsPerCta);
+              tma_load_3d(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
+                          half * 64, token, hg * kMaxDecodeHeadsPerCta);
             }
           }
         }
