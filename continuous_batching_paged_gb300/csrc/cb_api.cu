@@ -257,6 +257,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   a.KB = gcd_int(block_size, 16);
   a.KBp = gcd_int(block_size, 128);
   int dctas = options != nullptr ? options->decode_ctas : 0;
+  a.decode_auto = dctas <= 0 ? 1 : 0;
   if (dctas <= 0) dctas = ds->sm_count;
   if (dctas > CB_MAX_DECODE_CTAS) dctas = CB_MAX_DECODE_CTAS;
   a.decode_ctas = dctas;

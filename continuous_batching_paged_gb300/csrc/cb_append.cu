@@ -105,6 +105,47 @@ __device__ __forceinline__ void block_scan4(int v[4], int ex[4], int tot[4], int
   __syncthreads();
 }
 
+// Decode CTA count for a batch whose chunk pass runs beside the decode pass.  Model, fitted to
+// GB300 measurements of these kernels: decode on N SMs streams its bytes at
+// BW(N) = ((0.105 N)^-3 + 6.45^-3)^(-1/3) TB/s (linear in N until HBM saturates); the chunk pass
+// runs at ~6.6 TFLOP/s per SM on the other SMs meanwhile and on every SM afterwards.  The
+// choice is the largest N within 1% of the modelled minimum step time, so that the decode
+// pass keeps its bandwidth where the curve is flat.  Without chunk work all CTAs decode.
+// Called by one full warp; candidates N = 8, 16, ... are spread over the lanes, in fp32 (the
+// fp64 rate of this part is far too low for even this much arithmetic on one thread).
+__device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int max_ctas, long long tiles) {
+  const int lane = threadIdx.x & 31;
+  if (tiles <= 0) return 1;
+  const int cap = (int)(tiles < max_ctas ? tiles : max_ctas);
+  if (chunk_flops <= 0.f) return cap;
+  const float w_us = chunk_flops * (1.f / 6.6e6f);  // chunk work in SM-microseconds
+  const float b_mb = dec_bytes * 1e-6f;             // decode bytes / 1e6: MB / (TB/s) = us
+  const int n_cand = (cap + 7) / 8;
+  float t[2];
+  int n[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = lane + 32 * k;
+    n[k] = 8 * (i + 1) < cap ? 8 * (i + 1) : cap;
+    t[k] = 3.4e38f;
+    if (i < n_cand) {
+      const float lin = 0.105f * n[k], sat = 6.45f;
+      const float bw = rcbrtf(1.f / (lin * lin * lin) + 1.f / (sat * sat * sat));
+      const float td = b_mb / bw;
+      const float left = w_us - (float)(max_ctas - n[k]) * td;
+      t[k] = td + (left > 0.f ? left / max_ctas : 0.f);
+    }
+  }
+  float t_min = fminf(t[0], t[1]);
+  for (int o = 16; o > 0; o >>= 1) t_min = fminf(t_min, __shfl_xor_sync(0xffffffffu, t_min, o));
+  int best = 1;
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (t[k] <= 1.01f * t_min) best = best > n[k] ? best : n[k];
+  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  return best;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   __shared__ int sw[32][4];
   const WsLayout L = ws_layout(a.S, a.Hq, a.D);
@@ -120,6 +161,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   if (tid == 0) {
     if (a.cu_seqlens_q[0] != 0 || a.cu_seqlens_q[a.S] != a.T) report(a.err, kErrOutOfRange);
   }
+  __syncthreads();
+  float my_keys = 0.f, my_pairs = 0.f;  // work estimates for the decode / chunk balance
   int carry[4] = {0, 0, 0, 0};
   for (int base = 0; base < a.S; base += kPlanThreads) {
     const int s = base + tid;
@@ -134,8 +177,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
       } else if (q_len == 1) {
         v[0] = 1;
         v[1] = (kv + kDecodeTileKeys - 1) / kDecodeTileKeys;
+        my_keys += (float)kv;
       } else if (q_len > 1) {
         v[2] = 1;
+        my_pairs += (float)q_len * (float)(kv - q_len) + 0.5f * (float)q_len * (float)(q_len + 1);
         v[3] = (q_len + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);  // pairs of query tiles
       }
     }
@@ -166,8 +211,36 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   // capped at the tile count so that no CTA range is empty.
   const int n_dec = carry[0];
   const long long ntiles = carry[1];
-  const int N = (int)(ntiles < a.decode_ctas ? (ntiles > 0 ? ntiles : 1) : a.decode_ctas);
-  if (tid == 0) hdr->decode_ctas = N;
+  __shared__ int s_N;
+  __shared__ float s_red[2][kPlanThreads / 32];
+  // fixed-order reduction, so that the CTA count (and with it the rounding of the split-KV
+  // merge) is the same on every call with the same lengths
+  for (int o = 16; o > 0; o >>= 1) {
+    my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
+    my_pairs += __shfl_xor_sync(0xffffffffu, my_pairs, o);
+  }
+  if ((tid & 31) == 0) {
+    s_red[0][tid >> 5] = my_keys;
+    s_red[1][tid >> 5] = my_pairs;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float keys = 0.f, pairs = 0.f;
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+      keys += s_red[0][w];
+      pairs += s_red[1][w];
+    }
+    int n = (int)(ntiles < a.decode_ctas ? (ntiles > 0 ? ntiles : 1) : a.decode_ctas);
+    if (a.decode_auto)
+      n = choose_decode_ctas(keys * (float)(a.Hkv * a.D * 4), pairs * (float)(4 * a.D * a.Hq),
+                             a.decode_ctas, ntiles);
+    if (tid == 0) {
+      s_N = n;
+      hdr->decode_ctas = n;
+    }
+  }
+  __syncthreads();
+  const int N = s_N;
   // Merge counters of the decode pass: one per (decode sequence, KV head), zero at start.
   int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
   for (int i = tid; i < n_dec * a.Hkv; i += kPlanThreads) merge_cnt[i] = 0;

@@ -32,6 +32,7 @@ struct AttnArgs {
   int KB;              // rows per TMA box on the page pool, decode pass: gcd(bs, 16)
   int KBp;             // rows per TMA box on the page pool, chunk pass: gcd(bs, 128)
   int decode_ctas;     // CTAs of the decode pass (<= CB_MAX_DECODE_CTAS)
+  int decode_auto;     // 1: the planner picks how many of them work (decode / chunk balance)
   int prefill_ctas;    // persistent CTAs of the prefill pass
   float scale_log2;    // softmax scale * log2(e)
 };
