@@ -364,7 +364,7 @@ def main():
     table, cu, kvl = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
     out = torch.empty_like(q)
     ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
-                                       b.num_pages, b.max_blocks, b.block_size),
+                                       b.num_pages, b.max_blocks, b.block_size, b.num_tokens),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()

@@ -180,7 +180,7 @@ def kv_append(k_new, v_new, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens
 
 
 def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_blocks,
-                   block_size, num_tokens=0) -> int:
+                   block_size, num_tokens) -> int:
     dims = _dims(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_blocks)
     return int(library().cb_attention_workspace_size(ctypes.byref(dims), int(block_size)))
 

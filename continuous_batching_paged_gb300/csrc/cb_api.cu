@@ -164,7 +164,7 @@ const char* cb_last_error_message(void) { return t_last_error.c_str(); }
 
 size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size) {
   if (check_dims(dims, block_size) != CB_OK) return 0;
-  return cb::ws_layout(dims->num_seqs, dims->num_q_heads, dims->head_dim).total;
+  return cb::ws_layout(dims->num_seqs, dims->num_tokens, dims->num_q_heads, dims->head_dim).total;
 }
 
 cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
@@ -225,7 +225,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
     return fail(CB_ERR_INVALID_ARG, "lse must be 4-byte aligned");
   if (!(scale > 0.f) || scale != scale)
     return fail(CB_ERR_INVALID_ARG, "scale must be a positive finite number");
-  const size_t need = cb::ws_layout(dims->num_seqs, dims->num_q_heads, dims->head_dim).total;
+  const size_t need = cb::ws_layout(dims->num_seqs, dims->num_tokens, dims->num_q_heads, dims->head_dim).total;
   if (workspace_bytes < need)
     return fail(CB_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   const int Hq = dims->num_q_heads, Hkv = dims->num_kv_heads, G = Hq / Hkv;

@@ -146,9 +146,27 @@ __device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int max_ct
   return best;
 }
 
+// Histogram bin of chunk unit g (global index in chunk-sequence order): units that stream
+// more K/V tiles get lower bins, so an ascending walk over the bins is longest first.
+__device__ int pf_unit_bin(const AttnArgs& a, const int32_t* pf_seq, const int32_t* pf_prefix,
+                           int n_pf, int g) {
+  int lo = 0, hi = n_pf - 1;  // largest i with pf_prefix[i] <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pf_prefix[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  const int s = pf_seq[lo];
+  const int u = g - pf_prefix[lo];
+  const int q_len = a.cu_seqlens_q[s + 1] - a.cu_seqlens_q[s];
+  const int rows = min((u + 1) * pf_unit_tiles(a.G) * kPrefillTileM, q_len);
+  const int tiles = (a.kv_lens[s] - q_len + rows + kChunkKeys - 1) / kChunkKeys;
+  return kCostBins - 1 - min(tiles, kCostBins - 1);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
+  static_assert(kCostBins == kPlanThreads, "one histogram bin per planner thread");
   __shared__ int sw[32][4];
-  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
   int32_t* dec_seq = reinterpret_cast<int32_t*>(a.ws + L.dec_seq);
   int32_t* dec_prefix = reinterpret_cast<int32_t*>(a.ws + L.dec_prefix);
@@ -163,6 +181,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   }
   __syncthreads();
   float my_keys = 0.f, my_pairs = 0.f;  // work estimates for the decode / chunk balance
+  bool bad = false;
+  const int unit_rows = pf_unit_tiles(a.G) * kPrefillTileM;
   int carry[4] = {0, 0, 0, 0};
   for (int base = 0; base < a.S; base += kPlanThreads) {
     const int s = base + tid;
@@ -174,6 +194,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
       const bool ok = c0 >= 0 && c1 <= a.T && q_len >= 0 && kv >= q_len && kv <= max_kv;
       if (!ok) {
         report(a.err, kErrOutOfRange);
+        bad = true;
       } else if (q_len == 1) {
         v[0] = 1;
         v[1] = (kv + kDecodeTileKeys - 1) / kDecodeTileKeys;
@@ -181,7 +202,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
       } else if (q_len > 1) {
         v[2] = 1;
         my_pairs += (float)q_len * (float)(kv - q_len) + 0.5f * (float)q_len * (float)(q_len + 1);
-        v[3] = (q_len + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);  // pairs of query tiles
+        v[3] = (q_len + unit_rows - 1) / unit_rows;  // work units (pf_unit_tiles)
       }
     }
     int ex[4], tot[4];
@@ -197,16 +218,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) carry[k] += tot[k];
   }
+  // With every length valid the query ranges are disjoint, so the units fit pf_order (at most
+  // S + T / 128); after an invalid length the chunk pass is given no work.
+  bad = __syncthreads_or(bad) != 0;
+  const int n_pf = carry[2];
+  const int n_units = bad ? 0 : carry[3];
   if (tid == 0) {
     dec_prefix[carry[0]] = carry[1];
     pf_prefix[carry[2]] = carry[3];
     hdr->n_dec = carry[0];
     hdr->dec_tiles = carry[1];
-    hdr->n_pf = carry[2];
-    hdr->pf_qtiles = carry[3];
+    hdr->n_pf = n_pf;
+    hdr->pf_qtiles = n_units;
     hdr->pf_counter = 0;
   }
   __syncthreads();
+  // Chunk units longest first (a counting sort on the K/V tiles each streams, descending), so
+  // that the chunk CTAs, taking items in this order from a shared counter, schedule them
+  // longest-processing-time first.  Units of equal cost land in any order: each item writes
+  // its own output rows, so the order never changes a result.
+  {
+    __shared__ int hist[kCostBins];
+    int32_t* pf_order = reinterpret_cast<int32_t*>(a.ws + L.pf_order);
+    hist[tid] = 0;
+    __syncthreads();
+    for (int g = tid; g < n_units; g += kPlanThreads)
+      atomicAdd(&hist[pf_unit_bin(a, pf_seq, pf_prefix, n_pf, g)], 1);
+    __syncthreads();
+    int v[4] = {hist[tid], 0, 0, 0}, ex[4], tot[4];
+    block_scan4(v, ex, tot, sw);
+    hist[tid] = ex[0];
+    __syncthreads();
+    for (int g = tid; g < n_units; g += kPlanThreads)
+      pf_order[atomicAdd(&hist[pf_unit_bin(a, pf_seq, pf_prefix, n_pf, g)], 1)] = g;
+  }
   // First decode sequence of each decode CTA: CTA c owns tiles [c*n/N, (c+1)*n/N), with N
   // capped at the tile count so that no CTA range is empty.
   const int n_dec = carry[0];

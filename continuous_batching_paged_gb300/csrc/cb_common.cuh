@@ -20,14 +20,24 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 constexpr int kDecodeTileKeys = 16;     // keys per decode pipeline stage
 constexpr int kPrefillTileM = 128;      // queries per prefill tile (TMEM lanes)
+constexpr int kChunkKeys = 128;         // keys per K/V tile of the chunk pass
 constexpr int kMaxDecodeHeadsPerCta = 8;
+
+// A chunk-pass CTA runs two 128-query tiles A and B against the same K/V tiles.  With an even
+// GQA group size they are one query tile under two query heads of one KV group (equal key
+// ranges); otherwise two consecutive query tiles under one head.  A "unit" is what one item
+// covers under one head (pair): 1 tile or 2 tiles.
+__host__ __device__ inline bool pf_pair_heads(int G) { return (G & 1) == 0; }
+__host__ __device__ inline int pf_unit_tiles(int G) { return pf_pair_heads(G) ? 1 : 2; }
+
+constexpr int kCostBins = 1024;  // histogram bins of the planner's longest-first unit order
 
 // Workspace header (int32 words).
 struct PlanHeader {
   int32_t n_dec;          // number of decode sequences (q_len == 1)
   int32_t dec_tiles;      // total 16-key tiles over all decode sequences
   int32_t n_pf;           // number of chunk sequences (q_len > 1)
-  int32_t pf_qtiles;      // total pairs of 128-query tiles over all chunk sequences
+  int32_t pf_qtiles;      // total work units over all chunk sequences (pf_unit_tiles)
   int32_t pf_counter;     // dynamic work counter of the prefill pass (reset by the planner)
   int32_t decode_ctas;    // CTAs the decode pass was planned for
   int32_t pad[10];
@@ -35,13 +45,13 @@ struct PlanHeader {
 
 // Byte offsets of the workspace sections (all 256-byte aligned).
 struct WsLayout {
-  size_t header, dec_seq, dec_prefix, cta_first, pf_seq, pf_prefix, merge_cnt, part_ml, part_o,
-      total;
+  size_t header, dec_seq, dec_prefix, cta_first, pf_seq, pf_prefix, pf_order, merge_cnt, part_ml,
+      part_o, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WsLayout ws_layout(int S, int Hq, int D) {
+__host__ __device__ inline WsLayout ws_layout(int S, int T, int Hq, int D) {
   WsLayout L;
   size_t off = 0;
   L.header = off;     off = align_up(off + sizeof(PlanHeader), 256);
@@ -50,6 +60,8 @@ __host__ __device__ inline WsLayout ws_layout(int S, int Hq, int D) {
   L.cta_first = off;  off = align_up(off + sizeof(int32_t) * (size_t)(CB_MAX_DECODE_CTAS + 1), 256);
   L.pf_seq = off;     off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
   L.pf_prefix = off;  off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
+  // chunk units, longest first: at most one per 128 query tokens plus one per sequence
+  L.pf_order = off;   off = align_up(off + sizeof(int32_t) * ((size_t)S + (size_t)T / kPrefillTileM + 1), 256);
   L.merge_cnt = off;  off = align_up(off + sizeof(int32_t) * (size_t)S * (size_t)Hq, 256);
   const size_t slots = (size_t)CB_MAX_DECODE_CTAS + (size_t)S;
   L.part_ml = off;    off = align_up(off + sizeof(float2) * slots * (size_t)Hq, 256);

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
   const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, hg = blockIdx.y;
-  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
   const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
   const int32_t* dec_prefix = reinterpret_cast<const int32_t*>(a.ws + L.dec_prefix);

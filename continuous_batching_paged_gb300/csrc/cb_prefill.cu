@@ -4,10 +4,13 @@
 // cores.  A chunk of queries attends to a cache that already holds the earlier chunks: query i
 // of a chunk with prior context ctx sees keys 0 .. ctx + i (same section).
 //
-// One work item = (chunk sequence, pair of 128-query tiles A and B, query head).  Persistent
-// CTAs (one per SM) take items from a device counter the planner reset; items are ordered
-// longest first within a chunk and with the query head fastest, so the CTAs working on the
-// heads of one KV group at the same time share its K/V tiles through L2.  Per CTA,
+// One work item = two 128-query tiles A and B that read the same K/V tiles: with an even GQA
+// group size, one query tile of a chunk under two query heads of one KV group (equal key
+// ranges, so the two softmax groups stay in step); otherwise two consecutive query tiles under
+// one head.  Persistent CTAs (one per SM) take items from a device counter the planner reset,
+// in the planner's longest-first order of the work units with the query head (pair) fastest,
+// so the scheduling is longest-processing-time first and the CTAs working on the heads of one
+// KV group at the same time share its K/V tiles through L2.  Per CTA,
 // warp-specialised (12 warps, three warpgroups; setmaxnreg moves registers from the first
 // warpgroup, which only issues copies and MMAs, to the two softmax warpgroups: 104 + 2 x 200
 // per thread slot = the 3 x 168 the launch provides):
@@ -32,7 +35,6 @@
 
 namespace cb {
 
-constexpr int kChunkKeys = 128;    // keys per K/V tile of the chunk pass
 constexpr int kEntryCache = 1024;  // block-table entries of an item staged in shared memory
 
 template <int D>
@@ -66,41 +68,58 @@ static_assert(kRegsIssue + 2 * kRegsSoftmax <= 3 * 168, "register split exceeds 
 constexpr int kItemConsumers = 9;  // MMA thread + 4 warps of each softmax group
 
 struct PfItem {
-  int s, head, kvh, ctx;
-  int tok[2], rows[2], nk[2], nt[2];  // per tile: first token, valid rows, keys, K/V tiles
-  int nt_all, nk_all;                 // K/V tiles loaded and keys covered for the pair
+  int s, kvh, ctx;
+  int head[2], tok[2], rows[2], nk[2], nt[2];  // per tile: query head, first token, valid rows,
+                                               // keys, K/V tiles
+  int nt_all, nk_all;                          // K/V tiles loaded and keys covered for the item
   bool hasB;
 };
 
+// Query heads (pairs) per unit: items are unit-major with the head (pair) fastest, so the
+// CTAs on the heads of one KV group at the same time share its K/V tiles through L2.
+__device__ __forceinline__ int pf_heads_per_unit(const AttnArgs& a) {
+  return pf_pair_heads(a.G) ? a.Hq / 2 : a.Hq;
+}
+
 __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
                                                  const int32_t* pf_seq, const int32_t* pf_prefix,
-                                                 int n_pf) {
+                                                 const int32_t* pf_order, int n_pf) {
   PfItem it;
-  const int pg = item / a.Hq;  // global pair index
-  it.head = item - pg * a.Hq;
-  it.kvh = it.head / a.G;
-  int lo = 0, hi = n_pf - 1;  // largest i with pf_prefix[i] <= pg
+  const int hu_n = pf_heads_per_unit(a);
+  const int pos = item / hu_n;  // position in the longest-first unit order
+  const int hu = item - pos * hu_n;
+  const int g = pf_order[pos];  // unit index in chunk-sequence order
+  int lo = 0, hi = n_pf - 1;    // largest i with pf_prefix[i] <= g
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pf_prefix[mid] <= pg) lo = mid; else hi = mid - 1;
+    if (pf_prefix[mid] <= g) lo = mid; else hi = mid - 1;
   }
   it.s = pf_seq[lo];
+  const int u = g - pf_prefix[lo];
   const int c0 = a.cu_seqlens_q[it.s];
   const int q_len = a.cu_seqlens_q[it.s + 1] - c0;
   it.ctx = a.kv_lens[it.s] - q_len;
-  const int npairs = pf_prefix[lo + 1] - pf_prefix[lo];
-  const int p = npairs - 1 - (pg - pf_prefix[lo]);  // longest pairs of a chunk first
-  const int nqt = (q_len + kPrefillTileM - 1) / kPrefillTileM;
-  const int tA = 2 * p, tB = 2 * p + 1;
-  it.hasB = tB < nqt;
-  it.tok[0] = c0 + tA * kPrefillTileM;
-  it.tok[1] = it.tok[0] + kPrefillTileM;
-  it.rows[0] = min(kPrefillTileM, q_len - tA * kPrefillTileM);
-  it.rows[1] = it.hasB ? min(kPrefillTileM, q_len - tB * kPrefillTileM) : 0;
-  it.nk[0] = it.ctx + tA * kPrefillTileM + it.rows[0];
-  it.nk[1] = it.hasB ? it.ctx + tB * kPrefillTileM + it.rows[1] : 0;
-  it.nt[0] = (it.nk[0] + kChunkKeys - 1) / kChunkKeys;
-  it.nt[1] = (it.nk[1] + kChunkKeys - 1) / kChunkKeys;
+  int qt[2];
+  if (pf_pair_heads(a.G)) {  // one query tile, heads 2hu and 2hu+1 of one KV group
+    qt[0] = qt[1] = u;
+    it.head[0] = 2 * hu;
+    it.head[1] = 2 * hu + 1;
+    it.hasB = true;
+  } else {                   // query tiles 2u and 2u+1, one head
+    qt[0] = 2 * u;
+    qt[1] = 2 * u + 1;
+    it.head[0] = it.head[1] = hu;
+    it.hasB = qt[1] * kPrefillTileM < q_len;
+  }
+  it.kvh = it.head[0] / a.G;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const bool on = t == 0 || it.hasB;
+    it.tok[t] = c0 + qt[t] * kPrefillTileM;
+    it.rows[t] = on ? min(kPrefillTileM, q_len - qt[t] * kPrefillTileM) : 0;
+    it.nk[t] = on ? it.ctx + qt[t] * kPrefillTileM + it.rows[t] : 0;
+    it.nt[t] = (it.nk[t] + kChunkKeys - 1) / kChunkKeys;
+  }
   it.nk_all = max(it.nk[0], it.nk[1]);
   it.nt_all = max(it.nt[0], it.nt[1]);
   return it;
@@ -122,12 +141,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   volatile int* item_ids = reinterpret_cast<volatile int*>(smem + SM::kMisc + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WsLayout L = ws_layout(a.S, a.Hq, a.D);
+  const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
   const int32_t* pf_seq = reinterpret_cast<const int32_t*>(a.ws + L.pf_seq);
   const int32_t* pf_prefix = reinterpret_cast<const int32_t*>(a.ws + L.pf_prefix);
+  const int32_t* pf_order = reinterpret_cast<const int32_t*>(a.ws + L.pf_order);
   const int n_pf = hdr->n_pf;
-  const int n_items = hdr->pf_qtiles * a.Hq;  // pf_qtiles counts tile pairs
+  const int n_items = hdr->pf_qtiles * pf_heads_per_unit(a);
   if (n_items == 0) return;
 
   if (threadIdx.x == 0) {
@@ -184,7 +204,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item < 0) break;
-        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
+        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
         if (lane == 0) {
           if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
           mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kQTile);
@@ -192,7 +212,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
             for (int half = 0; half < SM::kHalves; ++half)
               tma_load_3d(sbase + SM::kQ0 + t * SM::kQTile + half * SM::kQHalf, &qmap,
-                          bar(SM::bQFull), half * 64, it.head, it.tok[t]);
+                          bar(SM::bQFull), half * 64, it.head[t], it.tok[t]);
         }
         const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
         // Stage the item's block-table entries in shared memory with coalesced loads issued
@@ -303,7 +323,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
         if (item < 0) break;
-        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
+        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
         const int nt_t[2] = {it.nt[0], it.hasB ? it.nt[1] : 0};
         wait(bar(SM::bQFull), k & 1);
         tc_fence_after();
@@ -365,7 +385,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
       if (item < 0) break;
-      const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, n_pf);
+      const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
       const uint32_t g_item = g;
       g += it.nt_all;
       if (t == 1 && !it.hasB) continue;
@@ -467,7 +487,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc_fence_after();
       const float inv = 1.f / l_run;
       const bool store = r < it.rows[t];
-      __nv_bfloat16* orow = outg + ((size_t)(it.tok[t] + r) * a.Hq + it.head) * D;
+      __nv_bfloat16* orow = outg + ((size_t)(it.tok[t] + r) * a.Hq + it.head[t]) * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t ov[32];
@@ -484,7 +504,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
       if (store && a.lse != nullptr)
-        a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head[t]] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(bar(SM::bOFree + t));
       gx += nt;

@@ -93,7 +93,9 @@ cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void
 /*
  * cb_attention_workspace_size -- bytes of device scratch cb_ragged_paged_attention needs.
  * Pure host arithmetic on (dims, block_size); 0 when dims is NULL or invalid.  The
- * workspace holds the batch plan and the fp32 partial results of split decode sequences.
+ * workspace holds the batch plan (including the longest-first order of the chunk work, one
+ * int32 per 128 query tokens plus one per sequence) and the fp32 partial results of split
+ * decode sequences; it grows with num_seqs, num_tokens, num_q_heads and head_dim.
  */
 size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size);
 

@@ -51,7 +51,8 @@ class DeviceBatch:
         ws = torch.full((cb.workspace_size(self.b.num_seqs, self.b.num_q_heads,
                                            self.b.num_kv_heads, self.b.head_dim,
                                            self.b.num_pages, self.b.max_blocks,
-                                           self.b.block_size),), 255, dtype=torch.uint8,
+                                           self.b.block_size, self.b.num_tokens),), 255,
+                                           dtype=torch.uint8,
                         device="cuda")
         return cb.ragged_paged_attention(workspace=ws, *(
             self.q, self.k_pages if k_pages is None else k_pages,

@@ -57,7 +57,7 @@ def test_chunks_small(cuda_lib, D, bs):
     _run_full(b)
 
 
-@pytest.mark.parametrize("G", [1, 4, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 16])
 def test_mixed_gqa_groups(cuda_lib, G):
     Hkv = 2 if G < 16 else 1
     q_lens = [1, 40, 0, 1, 129, 1]
@@ -65,6 +65,36 @@ def test_mixed_gqa_groups(cuda_lib, G):
     b = workloads.build_batch(q_lens, kv_lens, Hkv * G, Hkv, 128, 32, seed=300 + G,
                               name=f"mixed G{G}")
     _run_full(b)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_chunks_of_unequal_cost(cuda_lib, G):
+    # many chunk work units whose K/V extents differ (prior context 0 .. 3000, ragged tails):
+    # the chunk pass takes them longest first, in an order unrelated to the sequence order;
+    # G = 1 pairs two query tiles per CTA, G = 4 pairs two query heads of one KV group
+    q_lens = [300, 513, 129, 2, 700, 1, 256]
+    kv_lens = [300, 513 + 900, 129 + 3000, 2 + 17, 700 + 2000, 40, 256 + 128]
+    b = workloads.build_batch(q_lens, kv_lens, 2 * G, 2, 128, 64, seed=400 + G,
+                              name=f"unequal chunks G{G}")
+    _run_full(b)
+
+
+def test_invalid_length_reported_and_chunk_pass_skipped(cuda_lib):
+    # kv_len < q_len for the second chunk: reported, no fault, the chunk pass does no work and
+    # the valid decode sequence is still computed
+    b = workloads.build_batch([1, 40, 60], [70, 120, 90], 8, 2, 128, 16, seed=91)
+    db = DeviceBatch(b)
+    db.append()
+    assert cb.get_device_error() == cb.CB_OK
+    kv = b.kv_lens.copy()
+    kv[2] = 10
+    db.kv_lens = i32(kv)
+    out = db.attend()
+    assert cb.get_device_error() == cb.CB_ERR_OUT_OF_RANGE
+    kp, vp = oracle_append(b)
+    ref, _ = opa.ragged_paged_attention(b.q[:1], kp, vp, b.block_table[:1], b.cu_seqlens_q[:2],
+                                        b.kv_lens[:1], b.block_size, b.scale)
+    assert_close(out[:1].float().cpu().numpy(), ref, "decode row beside an invalid chunk")
 
 
 def test_many_kv_heads_two_head_groups(cuda_lib):
