@@ -11,50 +11,95 @@
 
 namespace cb {
 
-// One thread copies one 16-byte chunk of K and the same chunk of V.
-__global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
-  const int cpr = a.D / 8;                       // 16-byte chunks per (token, head) row
-  const long long per_tok = (long long)a.Hkv * cpr;
-  const long long total = (long long)a.T * per_tok;
+// One warp per new token: the warp finds the token's sequence with 32-way probes of
+// cu_seqlens_q (a few rounds instead of a binary search per 16-byte chunk), then each lane
+// moves its share of the token's K row and V row (all KV heads: Hkv * D bf16, contiguous in
+// both the input and the token-major pool), issuing every load before the first store.
+constexpr int kAppendThreads = 256;
+constexpr int kAppendMaxChunks = 8;  // 16-byte chunks per lane and tensor in flight
+
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int cpr = a.Hkv * a.D / 8;  // 16-byte chunks per token row
   const uint4* kn = static_cast<const uint4*>(a.k_new);
   const uint4* vn = static_cast<const uint4*>(a.v_new);
   uint4* kp = static_cast<uint4*>(a.k_pages);
   uint4* vp = static_cast<uint4*>(a.v_pages);
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(idx / per_tok);
-    const int rem = (int)(idx - (long long)t * per_tok);
-    // Sequence of token t: the last s with cu[s] <= t (cu is non-decreasing).
+  const int nwarps = gridDim.x * (kAppendThreads / 32);
+  for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
+    // Sequence of token t: the last s with cu[s] <= t (cu is non-decreasing).  Each round
+    // probes 32 increasing positions in (lo, hi]; the lanes whose probe is <= t form a prefix.
     int lo = 0, hi = a.S;
     while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+      const int span = hi - lo;
+      const int p = lo + 1 + (int)((long long)(span - 1) * lane / 31);
+      const unsigned le = __ballot_sync(0xffffffffu, __ldg(a.cu_seqlens_q + p) <= t);
+      const int k = le ? 31 - __clz(le) : -1;
+      const int pk = __shfl_sync(0xffffffffu, p, k < 0 ? 0 : k);
+      const int pn = __shfl_sync(0xffffffffu, p, k < 31 ? k + 1 : 31);
+      if (k < 0) {
+        hi = pk - 1;
+      } else {
+        lo = pk;
+        if (k < 31 && pn - 1 < hi) hi = pn - 1;
+      }
     }
     const int s = lo;
-    if (s >= a.S) { report(a.err, kErrOutOfRange); continue; }
+    if (s >= a.S) {
+      if (lane == 0) report(a.err, kErrOutOfRange);
+      continue;
+    }
     const int c0 = __ldg(a.cu_seqlens_q + s), c1 = __ldg(a.cu_seqlens_q + s + 1);
     const int q_len = c1 - c0;
     const int kv = __ldg(a.kv_lens + s);
-    if (t < c0 || t >= c1 || kv < q_len) { report(a.err, kErrOutOfRange); continue; }
+    if (t < c0 || t >= c1 || kv < q_len) {
+      if (lane == 0) report(a.err, kErrOutOfRange);
+      continue;
+    }
     const int pos = kv - q_len + (t - c0);
     const int lb = pos / a.bs;
-    if (lb >= a.max_blocks) { report(a.err, kErrOutOfRange); continue; }
+    if (lb >= a.max_blocks) {
+      if (lane == 0) report(a.err, kErrOutOfRange);
+      continue;
+    }
     const int blk = __ldg(a.block_table + (size_t)s * a.max_blocks + lb);
-    if (blk < 0 || blk >= a.P) { report(a.err, kErrOutOfRange); continue; }
+    if (blk < 0 || blk >= a.P) {
+      if (lane == 0) report(a.err, kErrOutOfRange);
+      continue;
+    }
     const long long slot = (long long)blk * a.bs + (pos - lb * a.bs);
-    const long long dst = slot * per_tok + rem;
-    kp[dst] = __ldg(kn + idx);
-    vp[dst] = __ldg(vn + idx);
+    const uint4* ks = kn + (size_t)t * cpr;
+    const uint4* vs = vn + (size_t)t * cpr;
+    uint4* kd = kp + (size_t)slot * cpr;
+    uint4* vd = vp + (size_t)slot * cpr;
+    for (int base = 0; base < cpr; base += 32 * kAppendMaxChunks) {
+      uint4 kr[kAppendMaxChunks], vr[kAppendMaxChunks];
+#pragma unroll
+      for (int i = 0; i < kAppendMaxChunks; ++i) {
+        const int c = base + lane + 32 * i;
+        if (c < cpr) {
+          kr[i] = __ldg(ks + c);
+          vr[i] = __ldg(vs + c);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kAppendMaxChunks; ++i) {
+        const int c = base + lane + 32 * i;
+        if (c < cpr) {
+          kd[c] = kr[i];
+          vd[c] = vr[i];
+        }
+      }
+    }
   }
 }
 
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
-  const long long total = (long long)a.T * a.Hkv * (a.D / 8);
-  if (total == 0) return cudaSuccess;
-  const int threads = 256;
-  long long blocks = (total + threads - 1) / threads;
-  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(a);
+  if (a.T == 0) return cudaSuccess;
+  const int warps = kAppendThreads / 32;
+  long long blocks = ((long long)a.T + warps - 1) / warps;
+  if (blocks > 8192) blocks = 8192;
+  kv_append_kernel<<<(unsigned)blocks, kAppendThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -64,58 +64,90 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
 // out = sum_c w_c o_c / sum_c w_c l_c, lse = (M + log2 sum_c w_c l_c) * ln 2.
 // Other CTAs wrote these parts: they are read through L2 (ld.global.cg), never from a stale L1
 // line.  Lane i first fetches (m, l) of part-head pair i, so all of them are read in one round
-// trip; the o loads of a head are then independent of each other.
+// trip; then the o rows of 2 heads x 4 parts are loaded together (one vector per lane
+// and row) before any is used, so the merge costs a few L2 round trips, not one per row.
 template <int D>
 __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* part_ml,
                                             const float* part_o, int dec, int tok, int kvh,
                                             int cf, int cl, int lane) {
-  constexpr int PER = D / 32;  // output columns per lane
+  constexpr int PER = D / 32;  // output columns per lane: 4 (D = 128) or 2 (D = 64)
+  constexpr int kH = 2, kC = 4;  // heads and parts in flight
   __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
   const int nparts = cl - cf + 1;
-  for (int r0 = 0; r0 < a.G; r0 += 32 / nparts > 0 ? 32 / nparts : 1) {
-    // lane -> (head r0 + lane / nparts, part lane % nparts)
-    const int rows_here = min(a.G - r0, max(32 / nparts, 1));
-    const int hr = lane / nparts, pc = lane % nparts;
+  const bool shfl = nparts <= 32;
+  const int rows_per_round = shfl ? 32 / nparts : a.G;
+  for (int r0 = 0; r0 < a.G; r0 += rows_per_round) {
+    const int rows_here = min(a.G - r0, rows_per_round);
+    const int hr = shfl ? lane / nparts : 0, pc = shfl ? lane % nparts : 0;
     float2 ml = make_float2(-INFINITY, 0.f);
-    if (nparts <= 32 && hr < rows_here)
+    if (shfl && hr < rows_here)
       ml = __ldcg(part_ml + ((size_t)(cf + pc) + dec) * a.Hq + kvh * a.G + r0 + hr);
-    for (int rr = 0; rr < rows_here; ++rr) {
-      const int head = kvh * a.G + r0 + rr;
-      float M = -INFINITY;
-      if (nparts <= 32) {
-        for (int cc = 0; cc < nparts; ++cc)
-          M = fmaxf(M, __shfl_sync(0xffffffffu, ml.x, rr * nparts + cc));
-      } else {
-        for (int cc = cf; cc <= cl; ++cc)
-          M = fmaxf(M, __ldcg(part_ml + ((size_t)cc + dec) * a.Hq + head).x);
+    // (m, l) of (row rr of this round, part cc): a shuffle, or a load past 32 parts
+    auto part_ml_of = [&](int rr, int cc) -> float2 {
+      if (shfl)
+        return make_float2(__shfl_sync(0xffffffffu, ml.x, rr * nparts + cc),
+                           __shfl_sync(0xffffffffu, ml.y, rr * nparts + cc));
+      return __ldcg(part_ml + ((size_t)(cf + cc) + dec) * a.Hq + kvh * a.G + r0 + rr);
+    };
+    for (int rr0 = 0; rr0 < rows_here; rr0 += kH) {
+      float M[kH], Lsum[kH], acc[kH][PER];
+#pragma unroll
+      for (int hh = 0; hh < kH; ++hh) {
+        M[hh] = -INFINITY;
+        Lsum[hh] = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[hh][i] = 0.f;
+        if (rr0 + hh < rows_here)
+          for (int cc = 0; cc < nparts; ++cc) M[hh] = fmaxf(M[hh], part_ml_of(rr0 + hh, cc).x);
       }
-      float Lsum = 0.f, acc[PER];
+      for (int c0 = 0; c0 < nparts; c0 += kC) {
+        float v[kH][kC][PER];
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-      for (int cc = 0; cc < nparts; ++cc) {
-        const size_t slot = (size_t)(cf + cc) + dec;
-        float mx, lx;
-        if (nparts <= 32) {
-          mx = __shfl_sync(0xffffffffu, ml.x, rr * nparts + cc);
-          lx = __shfl_sync(0xffffffffu, ml.y, rr * nparts + cc);
-        } else {
-          const float2 v = __ldcg(part_ml + slot * a.Hq + head);
-          mx = v.x;
-          lx = v.y;
-        }
-        const float w = fast_exp2(mx - M);
-        Lsum += lx * w;
-        const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
+        for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] += __ldcg(po + i) * w;
+          for (int cc = 0; cc < kC; ++cc) {
+            const int head = kvh * a.G + r0 + rr0 + hh;
+            const float* po =
+                part_o + (((size_t)(cf + c0 + cc) + dec) * a.Hq + head) * D + lane * PER;
+            if (rr0 + hh < rows_here && c0 + cc < nparts) {
+              if constexpr (PER == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(po));
+                v[hh][cc][0] = x.x; v[hh][cc][1] = x.y; v[hh][cc][2] = x.z; v[hh][cc][3] = x.w;
+              } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2*>(po));
+                v[hh][cc][0] = x.x; v[hh][cc][1] = x.y;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < PER; ++i) v[hh][cc][i] = 0.f;
+            }
+          }
+#pragma unroll
+        for (int hh = 0; hh < kH; ++hh)
+#pragma unroll
+          for (int cc = 0; cc < kC; ++cc) {
+            if (rr0 + hh < rows_here && c0 + cc < nparts) {
+              const float2 mlx = part_ml_of(rr0 + hh, c0 + cc);
+              const float w = fast_exp2(mlx.x - M[hh]);
+              Lsum[hh] += mlx.y * w;
+#pragma unroll
+              for (int i = 0; i < PER; ++i) acc[hh][i] += v[hh][cc][i] * w;
+            }
+          }
       }
-      const float inv = 1.f / Lsum;
-      uint32_t* dst =
-          reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
 #pragma unroll
-      for (int i = 0; i < PER / 2; ++i) dst[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-      if (lane == 0 && a.lse != nullptr)
-        a.lse[(size_t)tok * a.Hq + head] = (M + __log2f(Lsum)) * 0.6931471805599453f;
+      for (int hh = 0; hh < kH; ++hh) {
+        if (rr0 + hh >= rows_here) continue;
+        const int head = kvh * a.G + r0 + rr0 + hh;
+        const float inv = 1.f / Lsum[hh];
+        uint32_t* dst =
+            reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
+#pragma unroll
+        for (int i = 0; i < PER / 2; ++i)
+          dst[i] = pack_bf16x2(acc[hh][2 * i] * inv, acc[hh][2 * i + 1] * inv);
+        if (lane == 0 && a.lse != nullptr)
+          a.lse[(size_t)tok * a.Hq + head] = (M[hh] + __log2f(Lsum[hh])) * 0.6931471805599453f;
+      }
     }
   }
 }

@@ -34,6 +34,26 @@ def test_append_ragged_small(cuda_lib, bs, D):
     _check_pool(DeviceBatch(b), b)
 
 
+@pytest.mark.parametrize("Hkv", [1, 3, 32])
+def test_append_row_widths(cuda_lib, Hkv):
+    # a token row of Hkv * D bf16: narrower than one 16-byte chunk per lane (Hkv 1, D 64),
+    # not a multiple of the warp (Hkv 3), and wider than one pass of the warp (Hkv 32, D 128)
+    D = 64 if Hkv == 1 else 128
+    q_lens = [1, 70, 3, 1]
+    kv_lens = [40, 70, 19, 1]
+    b = workloads.build_batch(q_lens, kv_lens, Hkv, Hkv, D, 16, seed=60 + Hkv)
+    _check_pool(DeviceBatch(b), b)
+
+
+def test_append_many_sequences(cuda_lib):
+    # 3000 sequences: several rounds of the warp's 32-way search for a token's sequence
+    rng = np.random.default_rng(61)
+    q_lens = [int(x) for x in rng.integers(0, 4, 3000)]
+    kv_lens = [q + int(rng.integers(0, 40)) for q in q_lens]
+    b = workloads.build_batch(q_lens, kv_lens, 4, 2, 64, 16, seed=62)
+    _check_pool(DeviceBatch(b), b)
+
+
 def test_append_max_table_and_idempotent(cuda_lib):
     bs = 16
     b = workloads.build_batch([3, 1], [64, 64], 4, 2, 128, bs, seed=7, max_blocks=4)  # full tables
