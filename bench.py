@@ -10,7 +10,7 @@ one batch of the named set in which every step of the path runs.
 
 Prints ONE JSON line.  `value` is query tokens per second of the whole job, from device time
 (CUDA events on the launching stream) with inputs resident in HBM; L2 is flushed (a 512 MiB
-write) before every timed step.  `e2e` is the same metric through the Python API with the step's
+write, then a 512 MiB read) before every timed step.  `e2e` is the same metric through the Python API with the step's
 inputs copied from pinned host memory and the output copied back inside the timed region.
 `roofline` is the dominant kernel's algorithmic bytes (or FLOPs) per launch over its average
 device time, measured by events the library records around each kernel.  `cpu_baseline` is the
@@ -330,7 +330,7 @@ def workload_config(b: workloads.Batch, args):
             "query_tokens": b.num_tokens, "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
             "head_dim": b.head_dim, "block_size": b.block_size, "pages": b.num_pages,
             "seed": 1000 + WORKLOADS[args.workload],
-            "l2": "flushed before every timed step (512 MiB write); KV also exceeds L2",
+            "l2": "flushed before every timed step (512 MiB write, then 512 MiB read); KV also exceeds L2",
             "parallelism": f"replicas x{args.gpus}"}
 
 
@@ -367,6 +367,14 @@ def main():
                                        b.num_pages, b.max_blocks, b.block_size, b.num_tokens),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # Write 512 MiB (evicts everything the last step left in the 129 MB L2), then read
+        # another 512 MiB, so the step starts on an L2 holding neither its inputs nor dirty
+        # lines whose write-back would be charged to the step's own DRAM traffic.
+        flush.fill_(1.0)
+        flush_r.sum()
     stream = torch.cuda.current_stream()
 
     # ev_start / ev_end bracket the step on the launching stream; the library records its five
@@ -390,12 +398,12 @@ def main():
     sampler.start()
     t_start = time.perf_counter()
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush_l2()
         step(False)
     torch.cuda.synchronize()
     soak = 0
     while time.perf_counter() - t_start < 2.0:   # let the clock sampler see the GPU under load
-        flush.fill_(1.0)
+        flush_l2()
         step(False)
         soak += 1
         if soak % 50 == 0:
@@ -408,7 +416,7 @@ def main():
     wall0 = time.perf_counter()
     step_ms = 0.0
     for _ in range(args.steps):
-        flush.fill_(1.0)
+        flush_l2()
         ev_start.record()
         step(False)
         ev_end.record()
@@ -429,7 +437,7 @@ def main():
     acc = {n: 0.0 for n in spans}
     n_span = max(1, min(args.steps, 30))
     for _ in range(n_span):
-        flush.fill_(1.0)
+        flush_l2()
         ev_start.record()
         step(True)
         ev_end.record()
@@ -466,7 +474,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = 0.0
     for _ in range(args.steps):
-        flush.fill_(1.0)
+        flush_l2()
         e0.record()
         e2e_step()
         e1.record()
