@@ -208,9 +208,15 @@ __device__ int pf_unit_bin(const AttnArgs& a, const int32_t* pf_seq, const int32
   return kCostBins - 1 - min(tiles, kCostBins - 1);
 }
 
+// Batches of up to this many decode (or chunk) sequences keep the planner's prefix arrays in
+// shared memory as well, so its binary searches cost no global round trips.
+constexpr int kPlanSmemSeqs = 2048;
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   static_assert(kCostBins == kPlanThreads, "one histogram bin per planner thread");
   __shared__ int sw[32][4];
+  __shared__ int32_t s_dec_prefix[kPlanSmemSeqs + 1], s_pf_prefix[kPlanSmemSeqs + 1];
+  __shared__ int32_t s_pf_seq[kPlanSmemSeqs];
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
   int32_t* dec_seq = reinterpret_cast<int32_t*>(a.ws + L.dec_seq);
@@ -253,12 +259,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
     int ex[4], tot[4];
     block_scan4(v, ex, tot, sw);
     if (v[0]) {
-      dec_seq[carry[0] + ex[0]] = s;
-      dec_prefix[carry[0] + ex[0]] = carry[1] + ex[1];
+      const int i = carry[0] + ex[0];
+      dec_seq[i] = s;
+      dec_prefix[i] = carry[1] + ex[1];
+      if (i < kPlanSmemSeqs) s_dec_prefix[i] = carry[1] + ex[1];
     }
     if (v[2]) {
-      pf_seq[carry[2] + ex[2]] = s;
-      pf_prefix[carry[2] + ex[2]] = carry[3] + ex[3];
+      const int i = carry[2] + ex[2];
+      pf_seq[i] = s;
+      pf_prefix[i] = carry[3] + ex[3];
+      if (i < kPlanSmemSeqs) {
+        s_pf_seq[i] = s;
+        s_pf_prefix[i] = carry[3] + ex[3];
+      }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) carry[k] += tot[k];
@@ -271,6 +284,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   if (tid == 0) {
     dec_prefix[carry[0]] = carry[1];
     pf_prefix[carry[2]] = carry[3];
+    if (carry[0] <= kPlanSmemSeqs) s_dec_prefix[carry[0]] = carry[1];
+    if (carry[2] <= kPlanSmemSeqs) s_pf_prefix[carry[2]] = carry[3];
     hdr->n_dec = carry[0];
     hdr->dec_tiles = carry[1];
     hdr->n_pf = n_pf;
@@ -287,15 +302,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
     int32_t* pf_order = reinterpret_cast<int32_t*>(a.ws + L.pf_order);
     hist[tid] = 0;
     __syncthreads();
+    const bool pf_local = n_pf <= kPlanSmemSeqs;
+    const int32_t* ps = pf_local ? s_pf_seq : pf_seq;
+    const int32_t* pp = pf_local ? s_pf_prefix : pf_prefix;
     for (int g = tid; g < n_units; g += kPlanThreads)
-      atomicAdd(&hist[pf_unit_bin(a, pf_seq, pf_prefix, n_pf, g)], 1);
+      atomicAdd(&hist[pf_unit_bin(a, ps, pp, n_pf, g)], 1);
     __syncthreads();
     int v[4] = {hist[tid], 0, 0, 0}, ex[4], tot[4];
     block_scan4(v, ex, tot, sw);
     hist[tid] = ex[0];
     __syncthreads();
     for (int g = tid; g < n_units; g += kPlanThreads)
-      pf_order[atomicAdd(&hist[pf_unit_bin(a, pf_seq, pf_prefix, n_pf, g)], 1)] = g;
+      pf_order[atomicAdd(&hist[pf_unit_bin(a, ps, pp, n_pf, g)], 1)] = g;
   }
   // First decode sequence of each decode CTA: CTA c owns tiles [c*n/N, (c+1)*n/N), with N
   // capped at the tile count so that no CTA range is empty.
@@ -334,12 +352,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   // Merge counters of the decode pass: one per (decode sequence, KV head), zero at start.
   int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
   for (int i = tid; i < n_dec * a.Hkv; i += kPlanThreads) merge_cnt[i] = 0;
+  const int32_t* dp = n_dec <= kPlanSmemSeqs ? s_dec_prefix : dec_prefix;
   for (int c = tid; c <= N; c += kPlanThreads) {
     const long long t0 = ntiles * c / N;
     int lo = 0, hi = n_dec;  // largest d in [0, n_dec] with dec_prefix[d] <= t0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (dec_prefix[mid] <= t0) lo = mid; else hi = mid - 1;
+      if (dp[mid] <= t0) lo = mid; else hi = mid - 1;
     }
     cta_first[c] = lo;
   }

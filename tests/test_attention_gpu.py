@@ -97,6 +97,20 @@ def test_invalid_length_reported_and_chunk_pass_skipped(cuda_lib):
     assert_close(out[:1].float().cpu().numpy(), ref, "decode row beside an invalid chunk")
 
 
+def test_more_sequences_than_the_planner_keeps_on_chip(cuda_lib):
+    # 2100 decode and 2100 chunk sequences: past the 2048 the planner mirrors in shared memory,
+    # so its searches read the prefix arrays from the workspace
+    rng = np.random.default_rng(93)
+    n = 2100
+    q_lens = [1] * n + [2] * n
+    kv_lens = [int(x) for x in rng.integers(1, 40, n)] + [int(x) for x in rng.integers(2, 40, n)]
+    order = rng.permutation(2 * n)
+    q_lens = [q_lens[i] for i in order]
+    kv_lens = [kv_lens[i] for i in order]
+    b = workloads.build_batch(q_lens, kv_lens, 4, 2, 64, 16, seed=94, name="4200 seqs")
+    _run_full(b)
+
+
 def test_many_kv_heads_two_head_groups(cuda_lib):
     b = workloads.build_batch([1, 1, 70], [300, 45, 170], 32, 16, 128, 16, seed=17,
                               name="Hkv16")
