@@ -20,7 +20,7 @@ __all__ = [
     "CbError", "CB_OK", "CB_ERR_INVALID_ARG", "CB_ERR_UNSUPPORTED", "CB_ERR_OUT_OF_RANGE",
     "CB_ERR_TIMEOUT", "CB_ERR_CUDA", "CbDims", "CbOptions", "library", "library_path",
     "kv_append", "ragged_paged_attention", "workspace_size", "get_device_error",
-    "check_device_error", "status_string",
+    "check_device_error", "status_string", "copy_blocks", "kv_offload", "kv_restore",
 ]
 
 CB_OK = 0
@@ -91,6 +91,15 @@ def _declare(lib: ctypes.CDLL) -> None:
                                                       ctypes.POINTER(CbDims), _P]
     lib.cb_get_device_error.restype = ctypes.c_int
     lib.cb_get_device_error.argtypes = [_P]
+    lib.cb_copy_blocks.restype = ctypes.c_int
+    lib.cb_copy_blocks.argtypes = [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.POINTER(CbDims), _P]
+    lib.cb_kv_offload.restype = ctypes.c_int
+    lib.cb_kv_offload.argtypes = [_P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.POINTER(CbDims), _P, _P, _P]
+    lib.cb_kv_restore.restype = ctypes.c_int
+    lib.cb_kv_restore.argtypes = [_P, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.POINTER(CbDims), _P, _P, _P]
 
 
 def library(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -158,6 +167,57 @@ def _check_bf16(name, t, ndim):
     _require(t.dtype == torch.bfloat16, f"{name} must be bfloat16")
     _require(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     _require(t.dim() == ndim, f"{name} must have {ndim} dimensions")
+
+
+def _pool_dims(k_pages, v_pages, block_size) -> CbDims:
+    _check_bf16("k_pages", k_pages, 4)
+    _require(k_pages.shape == v_pages.shape, "v_pages must match k_pages")
+    P, bs, Hkv, D = k_pages.shape
+    _require(bs == block_size, "k_pages.shape[1] must be block_size")
+    return _dims(0, 0, Hkv, Hkv, D, P, 1)
+
+
+def _check_ids(name, t):
+    import torch
+    _require(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(),
+             f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def copy_blocks(k_pages, v_pages, src, dst, block_size, stream=None) -> None:
+    """Block dst[i] of both pools receives block src[i] (cb_copy_blocks: copy-on-write data)."""
+    dims = _pool_dims(k_pages, v_pages, block_size)
+    _check_ids("src", src)
+    _check_ids("dst", dst)
+    _require(src.numel() == dst.numel(), "src and dst must have the same length")
+    _check(library().cb_copy_blocks(_ptr(k_pages), _ptr(v_pages), _ptr(src), _ptr(dst),
+                                    src.numel(), int(block_size), ctypes.byref(dims),
+                                    _stream(stream)), "cb_copy_blocks")
+
+
+def kv_offload(k_pages, v_pages, blocks, block_size, host_k, host_v, stream=None) -> None:
+    """Gather blocks of both pools into pinned host tensors [n, bs, Hkv, D] (cb_kv_offload)."""
+    dims = _pool_dims(k_pages, v_pages, block_size)
+    _check_ids("blocks", blocks)
+    n = blocks.numel()
+    for name, h in (("host_k", host_k), ("host_v", host_v)):
+        _require(h.is_pinned() and h.is_contiguous() and h.numel() * h.element_size()
+                 >= n * k_pages[0].numel() * 2, f"{name} must be pinned, contiguous, large enough")
+    _check(library().cb_kv_offload(_ptr(k_pages), _ptr(v_pages), _ptr(blocks), n,
+                                   int(block_size), ctypes.byref(dims), _ptr(host_k),
+                                   _ptr(host_v), _stream(stream)), "cb_kv_offload")
+
+
+def kv_restore(k_pages, v_pages, blocks, block_size, host_k, host_v, stream=None) -> None:
+    """Scatter pinned host tensors [n, bs, Hkv, D] into blocks of both pools (cb_kv_restore)."""
+    dims = _pool_dims(k_pages, v_pages, block_size)
+    _check_ids("blocks", blocks)
+    n = blocks.numel()
+    for name, h in (("host_k", host_k), ("host_v", host_v)):
+        _require(h.is_pinned() and h.is_contiguous() and h.numel() * h.element_size()
+                 >= n * k_pages[0].numel() * 2, f"{name} must be pinned, contiguous, large enough")
+    _check(library().cb_kv_restore(_ptr(k_pages), _ptr(v_pages), _ptr(blocks), n,
+                                   int(block_size), ctypes.byref(dims), _ptr(host_k),
+                                   _ptr(host_v), _stream(stream)), "cb_kv_restore")
 
 
 def kv_append(k_new, v_new, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size,

@@ -35,7 +35,7 @@ def sources() -> list[str]:
 
 def _deps() -> list[str]:
     out = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
-    out.append(os.path.join(INCLUDE, "cb.h"))
+    out += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     out.append(os.path.abspath(__file__))
     return out
 

@@ -319,6 +319,65 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
                                       dims, nullptr, stream);
 }
 
+// Shared host half of the three block-move entry points.
+static cb_status block_move(const void* pk, const void* pv, void* dk, void* dv,
+                            const int32_t* src_idx, const int32_t* dst_idx, int32_t n,
+                            int32_t block_size, const cb_dims* dims, int mode, void* stream) {
+  t_last_error.clear();
+  if (dims == nullptr) return fail(CB_ERR_INVALID_ARG, "dims is NULL");
+  if (block_size < 4)
+    return fail(CB_ERR_INVALID_ARG, "block_size must be at least 4, got %d", block_size);
+  if (n < 0) return fail(CB_ERR_INVALID_ARG, "negative block count");
+  if (dims->num_kv_heads < 1 || dims->num_pages < 1)
+    return fail(CB_ERR_INVALID_ARG, "num_kv_heads and num_pages must be >= 1");
+  if (dims->head_dim != 64 && dims->head_dim != 128)
+    return fail(CB_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", dims->head_dim);
+  if (n == 0) return CB_OK;
+  if (!pk || !pv || !dk || !dv || (mode != cb::kMoveRestore && !src_idx) ||
+      (mode != cb::kMoveOffload && !dst_idx))
+    return fail(CB_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(pk) || !aligned16(pv) || !aligned16(dk) || !aligned16(dv))
+    return fail(CB_ERR_INVALID_ARG, "pools and host buffers must be 16-byte aligned");
+  DeviceState* ds = nullptr;
+  cb_status st = device_state(&ds);
+  if (st != CB_OK) return st;
+  cb::BlockMoveArgs a;
+  a.src[0] = static_cast<const char*>(pk);
+  a.src[1] = static_cast<const char*>(pv);
+  a.dst[0] = static_cast<char*>(dk);
+  a.dst[1] = static_cast<char*>(dv);
+  a.src_idx = src_idx;
+  a.dst_idx = dst_idx;
+  a.n = n;
+  a.P = dims->num_pages;
+  a.mode = mode;
+  a.block_bytes = (long long)block_size * dims->num_kv_heads * dims->head_dim * 2;
+  a.err = ds->err;
+  cudaError_t e = cb::launch_block_move(a, ds->sm_count, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block move launch");
+  return CB_OK;
+}
+
+cb_status cb_copy_blocks(void* k_pages, void* v_pages, const int32_t* src, const int32_t* dst,
+                         int32_t n, int32_t block_size, const cb_dims* dims, void* stream) {
+  return block_move(k_pages, v_pages, k_pages, v_pages, src, dst, n, block_size, dims,
+                    cb::kMoveCopy, stream);
+}
+
+cb_status cb_kv_offload(const void* k_pages, const void* v_pages, const int32_t* blocks,
+                        int32_t n, int32_t block_size, const cb_dims* dims, void* host_k,
+                        void* host_v, void* stream) {
+  return block_move(k_pages, v_pages, host_k, host_v, blocks, nullptr, n, block_size, dims,
+                    cb::kMoveOffload, stream);
+}
+
+cb_status cb_kv_restore(void* k_pages, void* v_pages, const int32_t* blocks, int32_t n,
+                        int32_t block_size, const cb_dims* dims, const void* host_k,
+                        const void* host_v, void* stream) {
+  return block_move(host_k, host_v, k_pages, v_pages, nullptr, blocks, n, block_size, dims,
+                    cb::kMoveRestore, stream);
+}
+
 cb_status cb_get_device_error(void* stream) {
   t_last_error.clear();
   DeviceState* ds = nullptr;

@@ -37,7 +37,21 @@ struct AttnArgs {
   float scale_log2;    // softmax scale * log2(e)
 };
 
+// Block moves: copy (pool -> pool), offload (pool -> linear host buffer), restore (host ->
+// pool).  Per pool (K, V) one block is block_bytes contiguous bytes.
+enum BlockMoveMode { kMoveCopy = 0, kMoveOffload = 1, kMoveRestore = 2 };
+struct BlockMoveArgs {
+  const char* src[2];   // K, V: pool (copy, offload) or host buffer (restore)
+  char* dst[2];         // K, V: pool (copy, restore) or host buffer (offload)
+  const int32_t* src_idx;  // block ids read (copy, offload)
+  const int32_t* dst_idx;  // block ids written (copy, restore)
+  int n, P, mode;
+  long long block_bytes;
+  uint32_t* err;
+};
+
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_block_move(const BlockMoveArgs& a, int sm_count, cudaStream_t stream);
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);

@@ -180,6 +180,42 @@ cb_status cb_ragged_paged_attention_noalloc(const void* q, const void* k_pages,
                                             const cb_dims* dims, void* stream);
 
 /*
+ * cb_copy_blocks -- copy whole KV blocks inside the page pools: for each i < n, block dst[i]
+ * of k_pages and of v_pages receives the content of block src[i] (bs * Hkv * D bf16 each).
+ * This is the data half of copy-on-write ("LLM learning path 3.3 Batching & Memory
+ * Management", section "PagedAttention: block tables": a sequence about to write into a block
+ * whose reference count is above 1 first copies it; section "Code": the real engine copies the
+ * KV data too); the block allocator (cb_sched.h) decides the pairs.
+ *   src, dst  device int32 [n]; k_pages, v_pages as in cb_kv_append (16-byte aligned).
+ *   dims      num_kv_heads, head_dim and num_pages are used; the other fields are ignored.
+ * Asynchronous on `stream`.  Pairs must not overlap (a block both read and written) — then
+ * the result is undefined.  A pair with a block id outside [0, num_pages) is skipped and
+ * reported through cb_get_device_error (CB_ERR_OUT_OF_RANGE); src == dst is a no-op.
+ */
+cb_status cb_copy_blocks(void* k_pages, void* v_pages, const int32_t* src, const int32_t* dst,
+                         int32_t n, int32_t block_size, const cb_dims* dims, void* stream);
+
+/*
+ * cb_kv_offload -- gather blocks[i] (i < n) of both pools into host_k and host_v, each laid
+ * out [n, bs, Hkv, D] bf16 (block i of the list at offset i * bs * Hkv * D); cb_kv_restore
+ * is the inverse scatter.  The batched copy of a request's blocks to a CPU tier and back
+ * (transformers "Continuous batching architecture", section "Memory management": offloaded
+ * requests' blocks go to CPU memory in one batched copy and come back the same way).
+ *   blocks           device int32 [n], ids in [0, num_pages)
+ *   host_k, host_v   host memory the device can address (pinned: cudaHostAlloc or
+ *                    cudaHostRegister), 16-byte aligned; owned by the caller, who must not
+ *                    touch it until the work on `stream` has completed.
+ * The kernel moves the bytes itself over the CPU-GPU link (no staging buffer, one launch for
+ * any number of blocks).  Out-of-range ids are skipped and reported as for cb_copy_blocks.
+ */
+cb_status cb_kv_offload(const void* k_pages, const void* v_pages, const int32_t* blocks,
+                        int32_t n, int32_t block_size, const cb_dims* dims, void* host_k,
+                        void* host_v, void* stream);
+cb_status cb_kv_restore(void* k_pages, void* v_pages, const int32_t* blocks, int32_t n,
+                        int32_t block_size, const cb_dims* dims, const void* host_k,
+                        const void* host_v, void* stream);
+
+/*
  * cb_get_device_error -- synchronise `stream`, then read and clear the current device's error
  * word.  Returns CB_OK, CB_ERR_OUT_OF_RANGE, CB_ERR_TIMEOUT (reported first when both were
  * seen) or CB_ERR_CUDA if the synchronisation itself failed.

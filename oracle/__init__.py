@@ -24,6 +24,12 @@ Pins (what each function is checked against, in tests/test_oracle_*.py):
   * ``batching``: the values "Continuous batching in transformers" and
     "LLM learning path 3.3" print (693 wasted slots, 670/2000, 1300/4000,
     63 blocks with 8 wasted slots, 32 x 256 = 8192, ...).
+  * ``scheduler``: the allocator demo of "LLM learning path 3.3", section "Code" (forked
+    samples copy the shared last block, the first block keeps count 2 after the parent is
+    freed), the 10,000-token / 1,500-token chunking example, the FIFO and PrefillFirst orders
+    of the transformers "Scheduler" section, and continuous batching = list scheduling on B
+    slots, fewer steps than static batching (tests/test_oracle_scheduler.py).
+  * ``blocks``: element-wise brute force on tiny pools (tests/test_oracle_blocks.py).
 No function here is "parity unpinned".
 """
 from .paged_attention import (  # noqa: F401
@@ -38,3 +44,5 @@ from .paged_attention import (  # noqa: F401
     attention_rows,
 )
 from . import batching  # noqa: F401
+from . import blocks  # noqa: F401
+from . import scheduler  # noqa: F401

@@ -10,7 +10,8 @@ import continuous_batching_paged_gb300 as cb
 from continuous_batching_paged_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "cb.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -20,15 +21,18 @@ def lib():
 
 
 def header_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cb_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(cb_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = header_functions()
     for required in ("cb_kv_append", "cb_ragged_paged_attention", "cb_attention_workspace_size",
-                     "cb_get_device_error", "cb_status_string"):
+                     "cb_get_device_error", "cb_status_string", "cb_copy_blocks", "cb_kv_offload",
+                     "cb_kv_restore", "cb_alloc_create", "cb_sched_step"):
         assert required in names
 
 
