@@ -59,6 +59,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--serial", action="store_true",
                    help="run the chunk kernel after the decode kernel instead of concurrently")
+    p.add_argument("--mode", choices=["path", "blocks", "serve"], default="path",
+                   help="path: the attention hot path (default); blocks: KV block copy / "
+                        "offload / restore kernels; serve: a scheduler-driven serving loop")
+    p.add_argument("--policy", choices=["fifo", "prefill_first"], default="fifo")
     return p.parse_args()
 
 
@@ -336,8 +340,195 @@ def workload_config(b: workloads.Batch, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def run_blocks(args, local: int):
+    """Block-move kernels on a 16384-block pool (bs 32, 8 KV heads, D 128: 64 KB per block and
+    pool): copy-on-write copies of 4096 disjoint block pairs inside HBM, and the offload /
+    restore of 4096 blocks to pinned host memory, each against its own roofline (the measured
+    HBM copy peak; a contiguous cudaMemcpy of the same bytes over the same CPU-GPU link)."""
+    import torch
+    import continuous_batching_paged_gb300 as cb
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P, bs, H, D, n = 16384, 32, 8, 128, 4096
+    kp = torch.randn((P, bs, H, D), device=dev).to(torch.bfloat16)
+    vp = torch.randn((P, bs, H, D), device=dev).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(1234)
+    perm = torch.randperm(P, generator=g)
+    src, dst = perm[:n].to(torch.int32).to(dev), perm[n:2 * n].to(torch.int32).to(dev)
+    blocks = perm[2 * n:3 * n].to(torch.int32).to(dev)
+    hk = torch.empty((n, bs, H, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((n, bs, H, D), dtype=torch.bfloat16).pin_memory()
+    block_bytes = bs * H * D * 2
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    dbuf = torch.empty((2 * n, bs, H, D), dtype=torch.bfloat16, device=dev)
+    hbuf = torch.empty((2 * n, bs, H, D), dtype=torch.bfloat16).pin_memory()
+
+    def timed(fn, reps):
+        e0, e1 = _events(torch, 2)
+        tot = 0.0
+        for i in range(args.warmup + reps):
+            flush.fill_(1.0)
+            flush_r.sum()
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            if i >= args.warmup:
+                tot += e0.elapsed_time(e1)
+        return tot / reps / 1e3  # seconds
+
+    reps = max(3, min(args.steps, 20))
+    t_copy = timed(lambda: cb.copy_blocks(kp, vp, src, dst, bs), reps)
+    t_off = timed(lambda: cb.kv_offload(kp, vp, blocks, bs, hk, hv), reps)
+    t_res = timed(lambda: cb.kv_restore(kp, vp, blocks, bs, hk, hv), reps)
+    t_d2h = timed(lambda: hbuf.copy_(dbuf, non_blocking=True), reps)
+    t_h2d = timed(lambda: dbuf.copy_(hbuf, non_blocking=True), reps)
+    cb.check_device_error()
+    pk, pk_kind = peaks()
+    moved = 2 * n * block_bytes                      # K and V blocks
+    copy_gbs = 2 * moved / t_copy / 1e9              # read + write
+    line = {
+        "metric": "KV block moves GB/s (copy-on-write copy in HBM; offload / restore over the "
+                  "CPU-GPU link)", "mode": "blocks", "n_gpus": 1, "data": "synthetic",
+        "config": {"pool_blocks": P, "block_size": bs, "kv_heads": H, "head_dim": D,
+                   "blocks_per_call": n, "bytes_per_call_each_way": moved,
+                   "l2": "flushed before every timed call (512 MiB write, then 512 MiB read)"},
+        "copy_blocks": {"ms": t_copy * 1e3, "gbs": copy_gbs, "peak_gbs": pk["hbm_gbs"],
+                        "frac": copy_gbs / pk["hbm_gbs"], "peak_kind": pk_kind + " HBM copy"},
+        "kv_offload": {"ms": t_off * 1e3, "gbs": moved / t_off / 1e9,
+                       "contiguous_d2h_gbs": moved / t_d2h / 1e9,
+                       "frac_of_contiguous": t_d2h / t_off},
+        "kv_restore": {"ms": t_res * 1e3, "gbs": moved / t_res / 1e9,
+                       "contiguous_h2d_gbs": moved / t_h2d / 1e9,
+                       "frac_of_contiguous": t_h2d / t_res},
+        "gpu_launches": 3 * reps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_serve(args, local: int):
+    """A continuous-batching serving loop driven by the native scheduler: 1024 requests
+    (prompt lognormal, median 512, sigma 1, capped at 4096; 64-512 new tokens), all queued at
+    the start, FIFO (or PrefillFirst) under max_batch_tokens 2048 and 256 requests per step on
+    a 64k-block pool (bs 32, 32 query / 8 KV heads, D 128).  Every step: the scheduler builds
+    the batch on the host, its metadata goes to the device from pinned buffers, then the
+    block copies, the KV append and the attention pass run.  Query/key/value rows come from a
+    pre-drawn random buffer (no model).  Reports query tokens per second of the whole loop
+    (host scheduling and launches included), the device time per step, and the host time of
+    the scheduler per step."""
+    import numpy as np
+    import torch
+    import continuous_batching_paged_gb300 as cb
+    from continuous_batching_paged_gb300.runtime import BlockAllocator, Scheduler
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    P, bs, Hq, Hkv, D, MB = 65536, 32, 32, 8, 128, 160
+    budget, cap = 2048, 256
+    rng = np.random.default_rng(2024)
+    n_req = 1024
+    prompts = np.minimum(np.exp(np.log(512) + rng.standard_normal(n_req)), 4096).astype(int) + 1
+    news = rng.integers(64, 513, n_req)
+    alloc = BlockAllocator(P, bs, MB)
+    sched = Scheduler(alloc, budget, cap, args.policy)
+    for i in range(n_req):
+        sched.add_request(i, int(prompts[i]), int(news[i]))
+    kp = torch.zeros((P, bs, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros((P, bs, Hkv, D), dtype=torch.bfloat16, device=dev)
+    q_all = torch.randn((budget, Hq, D), device=dev).to(torch.bfloat16)
+    k_all = torch.randn((budget, Hkv, D), device=dev).to(torch.bfloat16)
+    v_all = torch.randn((budget, Hkv, D), device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q_all)
+    ws = torch.empty(cb.workspace_size(cap, Hq, Hkv, D, P, MB, bs, budget), dtype=torch.uint8,
+                     device=dev)
+    nbuf = 3  # pinned metadata ring: the host fills step k+1 while the GPU reads step k
+    h_meta = [torch.empty(cap + 1 + cap + cap * MB + 2 * cap, dtype=torch.int32).pin_memory()
+              for _ in range(nbuf)]
+    d_meta = [torch.empty(cap + 1 + cap + cap * MB + 2 * cap, dtype=torch.int32, device=dev)
+              for _ in range(nbuf)]
+    done_ev = [None] * nbuf
+    stream = torch.cuda.current_stream()
+    lib = cb.library()
+    scale = 1.0 / float(np.sqrt(D))
+
+    def one_step(k):
+        t0 = time.perf_counter()
+        st = sched.step()
+        t_sched = time.perf_counter() - t0
+        S, T = len(st["seq_ids"]), int(st["num_tokens"])
+        if S == 0:
+            return 0, t_sched
+        slot = k % nbuf
+        if done_ev[slot] is not None:
+            done_ev[slot].synchronize()
+        h = h_meta[slot].numpy()
+        o = 0
+        h[o:o + S + 1] = st["cu_seqlens_q"]; cu_o = o; o += cap + 1
+        h[o:o + S] = st["kv_lens"]; kv_o = o; o += cap
+        h[o:o + S * MB] = st["block_table"].reshape(-1); tb_o = o; o += cap * MB
+        nc = len(st["cow_src"])
+        h[o:o + nc] = st["cow_src"]; src_o = o; o += cap
+        h[o:o + nc] = st["cow_dst"]; dst_o = o
+        d = d_meta[slot]
+        d.copy_(h_meta[slot], non_blocking=True)
+        cu_d, kv_d = d[cu_o:cu_o + S + 1], d[kv_o:kv_o + S]
+        tb_d = d[tb_o:tb_o + S * MB].view(S, MB)
+        if nc:
+            cb.copy_blocks(kp, vp, d[src_o:src_o + nc], d[dst_o:dst_o + nc], bs)
+        cb.kv_append(k_all[:T], v_all[:T], kp, vp, tb_d, cu_d, kv_d, bs)
+        cb.ragged_paged_attention(q_all[:T], kp, vp, tb_d, cu_d, kv_d, bs, scale,
+                                  out=out[:T], workspace=ws)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done_ev[slot] = ev
+        return T, t_sched
+
+    warm = max(3, args.warmup)
+    for k in range(warm):
+        one_step(k)
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    tokens, steps, t_sched = 0, 0, 0.0
+    limit = max(args.steps, 50)
+    wall0 = time.perf_counter()
+    e0.record()
+    while steps < limit and sched.num_active():
+        T, ts = one_step(warm + steps)
+        tokens += T
+        t_sched += ts
+        steps += 1
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    cb.check_device_error()
+    dev_ms = e0.elapsed_time(e1)
+    line = {
+        "metric": "continuous-batching loop query tokens/s (native scheduler + append + attention)",
+        "mode": "serve", "policy": args.policy, "n_gpus": 1, "data": "synthetic",
+        "value": tokens / wall, "unit": "query tokens/s", "steps": steps,
+        "tokens": tokens, "wall_ms_per_step": 1e3 * wall / steps,
+        "device_ms_per_step": dev_ms / steps,
+        "sched_us_per_step": 1e6 * t_sched / steps,
+        "config": {"requests": n_req, "prompt": "lognormal median 512 sigma 1 cap 4096",
+                   "new_tokens": "U[64, 512]", "max_batch_tokens": budget,
+                   "max_requests_per_batch": cap, "pool_blocks": P, "block_size": bs,
+                   "q_heads": Hq, "kv_heads": Hkv, "head_dim": D},
+        "gpu_launches": "5 per step (append, plan, decode, chunk; block copy when needed)",
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.mode != "path":
+        world, rank, local = dist_setup(args)
+        if rank == 0:
+            (run_blocks if args.mode == "blocks" else run_serve)(args, local)
+        return
     world, rank, local = dist_setup(args)
     cfg = WORKLOADS[args.workload]
     b = workloads.make_config(cfg, seed=1000 + cfg + 7919 * rank)
