@@ -14,7 +14,9 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <set>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "cb_sched.h"
@@ -37,22 +39,73 @@ cb_status fail(cb_status st, const char* fmt, ...) {
 
 struct SeqBlocks {
   std::vector<int32_t> blocks;
-  int32_t len = 0;  // tokens held
+  int32_t len = 0;     // tokens held
+  int32_t hashed = 0;  // leading blocks whose content hash chain is known
+  uint64_t chain = 0;  // hash of block hashed - 1 (0 before the first)
 };
+
+// Content hash of one full block chained with the hash of everything before it: 64-bit
+// FNV-1a over the parent hash's 8 bytes, then each token id's 4 bytes, little-endian.
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t n) {
+  uint64_t h = 14695981039346656037ull;
+  auto mix = [&](uint64_t x, int bytes) {
+    for (int i = 0; i < bytes; ++i) {
+      h ^= (x >> (8 * i)) & 0xffu;
+      h *= 1099511628211ull;
+    }
+  };
+  mix(parent, 8);
+  for (int32_t i = 0; i < n; ++i) mix((uint32_t)tokens[i], 4);
+  return h;
+}
 
 }  // namespace
 
 struct cb_alloc {
   int32_t num_blocks = 0, bs = 0, max_blocks = 0;
-  std::vector<int32_t> free_stack;  // top = back
+  std::vector<int32_t> free_stack;  // blocks without cached content; top = back
   std::vector<int32_t> ref;
   std::unordered_map<int32_t, SeqBlocks> seqs;
+  // Prefix cache ("Continuous batching architecture", sections "Prefix caching" and
+  // "Eviction"): every completed prompt block gets a content hash; a free block keeps its
+  // content and hash ("initialized") until an allocation finds no block without content, and
+  // then the most recently initialized free block is demoted (its hash dropped) and reused.
+  bool prefix = false;
+  std::vector<uint64_t> bhash;                    // 0: no cached content
+  std::vector<uint64_t> bparent;                  // chain hash before the block
+  std::vector<std::vector<int32_t>> btokens;      // the block's token ids
+  std::vector<int64_t> stamp;                     // order of initialization
+  std::unordered_map<uint64_t, int32_t> by_hash;  // content hash -> block
+  std::set<std::pair<int64_t, int32_t>> init_free;  // (stamp, block), free and initialized
+  int64_t next_stamp = 1;
 
+  int32_t free_count() const { return (int32_t)(free_stack.size() + init_free.size()); }
+  void drop_hash(int32_t b) {
+    auto it = by_hash.find(bhash[b]);
+    if (it != by_hash.end() && it->second == b) by_hash.erase(it);
+    bhash[b] = 0;
+  }
   int32_t pop() {
-    const int32_t b = free_stack.back();
-    free_stack.pop_back();
+    int32_t b;
+    if (!free_stack.empty()) {
+      b = free_stack.back();
+      free_stack.pop_back();
+    } else {
+      auto last = std::prev(init_free.end());  // the most recently initialized free block
+      b = last->second;
+      init_free.erase(last);
+      drop_hash(b);
+    }
     ref[b] = 1;
     return b;
+  }
+  void release(int32_t b) {  // reference count reached 0
+    if (prefix && bhash[b] != 0) init_free.insert({stamp[b], b});
+    else free_stack.push_back(b);
+  }
+  void retain(int32_t b) {  // a cached block is taken by one more sequence
+    if (ref[b] == 0) init_free.erase({stamp[b], b});
+    ref[b] += 1;
   }
   static int32_t blocks_for(int64_t tokens, int32_t bs) { return (int32_t)((tokens + bs - 1) / bs); }
   // Blocks growing `sq` by n tokens takes: new blocks past the last one, plus one copy when
@@ -72,6 +125,7 @@ struct cb_sched {
     int32_t done = 0;       // prompt tokens already in the cache
     int32_t generated = 0;  // tokens produced so far
     State state = kWaiting;
+    std::vector<int32_t> tokens;  // prompt token ids (prefix caching), may be empty
   };
   cb_alloc* alloc = nullptr;
   cb_sched_config cfg{};
@@ -98,6 +152,10 @@ cb_status cb_alloc_create(int32_t num_blocks, int32_t block_size, int32_t max_bl
   a->free_stack.resize(num_blocks);
   for (int32_t i = 0; i < num_blocks; ++i) a->free_stack[i] = i;  // block num_blocks-1 on top
   a->ref.assign(num_blocks, 0);
+  a->bhash.assign(num_blocks, 0);
+  a->bparent.assign(num_blocks, 0);
+  a->btokens.resize(num_blocks);
+  a->stamp.assign(num_blocks, 0);
   *out = a;
   return CB_OK;
 }
@@ -111,9 +169,9 @@ cb_status cb_alloc_add_seq(cb_alloc* a, int32_t seq, int32_t n_tokens) {
   if (nb > a->max_blocks)
     return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_add_seq: %d blocks exceed max_blocks_per_seq %d", nb,
                 a->max_blocks);
-  if (nb > (int32_t)a->free_stack.size())
-    return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_add_seq: %d blocks needed, %zu free", nb,
-                a->free_stack.size());
+  if (nb > a->free_count())
+    return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_add_seq: %d blocks needed, %d free", nb,
+                a->free_count());
   SeqBlocks sq;
   sq.len = n_tokens;
   sq.blocks.reserve(nb);
@@ -142,9 +200,9 @@ cb_status cb_alloc_append(cb_alloc* a, int32_t seq, int32_t n_tokens, int32_t* c
     return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_append: %d blocks exceed max_blocks_per_seq %d",
                 total, a->max_blocks);
   const int32_t need = a->needed(sq, n_tokens);
-  if (need > (int32_t)a->free_stack.size())
-    return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_append: %d blocks needed, %zu free", need,
-                a->free_stack.size());
+  if (need > a->free_count())
+    return fail(CB_ERR_OUT_OF_RANGE, "cb_alloc_append: %d blocks needed, %d free", need,
+                a->free_count());
   if (sq.len % a->bs != 0 && a->ref[sq.blocks.back()] > 1) {
     if (cow_src == nullptr || cow_dst == nullptr)
       return fail(CB_ERR_INVALID_ARG, "cb_alloc_append: a copy-on-write is needed but no output");
@@ -178,13 +236,83 @@ cb_status cb_alloc_free_seq(cb_alloc* a, int32_t seq) {
   if (it == a->seqs.end()) return fail(CB_ERR_INVALID_ARG, "cb_alloc_free_seq: no sequence %d", seq);
   for (int32_t b : it->second.blocks) {
     a->ref[b] -= 1;
-    if (a->ref[b] == 0) a->free_stack.push_back(b);
+    if (a->ref[b] == 0) a->release(b);
   }
   a->seqs.erase(it);
   return CB_OK;
 }
 
-int32_t cb_alloc_num_free(const cb_alloc* a) { return a ? (int32_t)a->free_stack.size() : 0; }
+int32_t cb_alloc_num_free(const cb_alloc* a) { return a ? a->free_count() : 0; }
+
+cb_status cb_alloc_set_prefix_caching(cb_alloc* a, int32_t enable) {
+  if (a == nullptr) return fail(CB_ERR_INVALID_ARG, "cb_alloc_set_prefix_caching: NULL");
+  if (!a->seqs.empty())
+    return fail(CB_ERR_INVALID_ARG, "cb_alloc_set_prefix_caching: set it before any sequence");
+  a->prefix = enable != 0;
+  return CB_OK;
+}
+
+int32_t cb_alloc_num_cached(const cb_alloc* a) { return a ? (int32_t)a->by_hash.size() : 0; }
+
+cb_status cb_alloc_add_seq_cached(cb_alloc* a, int32_t seq, const int32_t* tokens,
+                                  int32_t n_tokens, int32_t* n_cached) {
+  if (n_cached != nullptr) *n_cached = 0;
+  if (a == nullptr || n_tokens < 1 || tokens == nullptr)
+    return fail(CB_ERR_INVALID_ARG, "cb_alloc_add_seq_cached: bad argument");
+  if (a->seqs.count(seq))
+    return fail(CB_ERR_INVALID_ARG, "cb_alloc_add_seq_cached: sequence %d exists", seq);
+  SeqBlocks sq;
+  if (a->prefix) {
+    // Longest chain of cached full blocks, leaving at least the last token to compute.
+    const int32_t full = (n_tokens - 1) / a->bs;
+    uint64_t h = 0;
+    for (int32_t j = 0; j < full && j < a->max_blocks; ++j) {
+      const int32_t* tk = tokens + (size_t)j * a->bs;
+      const uint64_t hj = block_hash(h, tk, a->bs);
+      auto it = a->by_hash.find(hj);
+      if (it == a->by_hash.end()) break;
+      const int32_t b = it->second;
+      if (a->bparent[b] != h || std::memcmp(a->btokens[b].data(), tk, sizeof(int32_t) * a->bs))
+        break;  // a hash collision: not this content
+      a->retain(b);
+      sq.blocks.push_back(b);
+      h = hj;
+    }
+    sq.len = (int32_t)sq.blocks.size() * a->bs;
+    sq.hashed = (int32_t)sq.blocks.size();
+    sq.chain = h;
+  }
+  if (n_cached != nullptr) *n_cached = sq.len;
+  a->seqs.emplace(seq, std::move(sq));
+  return CB_OK;
+}
+
+cb_status cb_alloc_hash_blocks(cb_alloc* a, int32_t seq, const int32_t* tokens, int32_t n_tokens) {
+  if (a == nullptr) return fail(CB_ERR_INVALID_ARG, "cb_alloc_hash_blocks: NULL allocator");
+  auto it = a->seqs.find(seq);
+  if (it == a->seqs.end()) return fail(CB_ERR_INVALID_ARG, "cb_alloc_hash_blocks: no sequence %d", seq);
+  if (!a->prefix) return CB_OK;
+  SeqBlocks& sq = it->second;
+  if (n_tokens > sq.len || (n_tokens > 0 && tokens == nullptr))
+    return fail(CB_ERR_INVALID_ARG, "cb_alloc_hash_blocks: %d tokens, sequence holds %d", n_tokens,
+                sq.len);
+  const int32_t full = n_tokens / a->bs;
+  for (int32_t j = sq.hashed; j < full; ++j) {
+    const int32_t b = sq.blocks[j];
+    const int32_t* tk = tokens + (size_t)j * a->bs;
+    const uint64_t hj = block_hash(sq.chain, tk, a->bs);
+    if (a->bhash[b] == 0 && a->ref[b] == 1 && !a->by_hash.count(hj)) {
+      a->bhash[b] = hj;
+      a->bparent[b] = sq.chain;
+      a->btokens[b].assign(tk, tk + a->bs);
+      a->stamp[b] = a->next_stamp++;
+      a->by_hash[hj] = b;
+    }
+    sq.chain = hj;
+    sq.hashed = j + 1;
+  }
+  return CB_OK;
+}
 
 int32_t cb_alloc_ref_count(const cb_alloc* a, int32_t block) {
   if (a == nullptr || block < 0 || block >= a->num_blocks) return -1;
@@ -243,6 +371,15 @@ cb_status cb_sched_add_request(cb_sched* s, int32_t id, int32_t prompt_len,
   return CB_OK;
 }
 
+cb_status cb_sched_add_request_tokens(cb_sched* s, int32_t id, const int32_t* tokens,
+                                      int32_t prompt_len, int32_t max_new_tokens) {
+  if (tokens == nullptr) return fail(CB_ERR_INVALID_ARG, "cb_sched_add_request_tokens: NULL tokens");
+  const cb_status st = cb_sched_add_request(s, id, prompt_len, max_new_tokens);
+  if (st != CB_OK) return st;
+  s->reqs.back().tokens.assign(tokens, tokens + prompt_len);
+  return CB_OK;
+}
+
 cb_status cb_sched_fork_request(cb_sched* s, int32_t parent, int32_t child,
                                 int32_t max_new_tokens) {
   if (s == nullptr) return fail(CB_ERR_INVALID_ARG, "cb_sched_fork_request: NULL scheduler");
@@ -285,6 +422,7 @@ cb_status cb_sched_step(cb_sched* s, cb_batch* out) {
     return fail(CB_ERR_INVALID_ARG, "cb_sched_step: output arrays missing or too small");
   cb_alloc* A = s->alloc;
   out->num_seqs = out->num_tokens = out->num_cow = out->num_decode = out->num_finished = 0;
+  out->num_cached = 0;
   out->cu_seqlens_q[0] = 0;
 
   // Retire the requests that produced all their tokens last step.
@@ -300,8 +438,8 @@ cb_status cb_sched_step(cb_sched* s, cb_batch* out) {
   // Admit `n` tokens of request r; false (nothing changes) when the blocks do not suffice.
   auto admit = [&](cb_sched::Request& r, int32_t n) -> bool {
     if (n <= 0) return false;
-    const bool fresh = r.state == cb_sched::kWaiting;
-    if (cb_alloc_blocks_needed(A, r.id, n) > (int32_t)A->free_stack.size()) return false;
+    const bool fresh = !A->seqs.count(r.id);
+    if (cb_alloc_blocks_needed(A, r.id, n) > A->free_count()) return false;
     if (fresh) {
       if (cb_alloc_add_seq(A, r.id, n) != CB_OK) return false;
     } else {
@@ -334,6 +472,7 @@ cb_status cb_sched_step(cb_sched* s, cb_batch* out) {
     } else {
       r.done += n;
       r.state = cb_sched::kPrefill;
+      if (A->prefix && !r.tokens.empty()) cb_alloc_hash_blocks(A, r.id, r.tokens.data(), r.done);
       if (r.done == r.prompt) {
         r.state = cb_sched::kDecode;
         r.generated = 1;  // the last prompt position gives the first token
@@ -349,7 +488,7 @@ cb_status cb_sched_step(cb_sched* s, cb_batch* out) {
     if (n > budget) n = budget;
     int64_t fit;
     auto it = A->seqs.find(r.id);
-    const int64_t free_blocks = (int64_t)A->free_stack.size();
+    const int64_t free_blocks = (int64_t)A->free_count();
     if (it == A->seqs.end()) {
       fit = std::min<int64_t>(free_blocks, A->max_blocks) * A->bs;
     } else {
@@ -375,6 +514,18 @@ cb_status cb_sched_step(cb_sched* s, cb_batch* out) {
       if (start[i] != want || r.state != want) continue;
       if (want == cb_sched::kDecode) {
         if (r.generated < r.max_new) admit(r, 1);
+      } else if (want == cb_sched::kWaiting && A->prefix && !r.tokens.empty()) {
+        // Prefix caching: start from the longest cached chain of full prompt blocks; the
+        // chunk then covers the rest.  Nothing changes if no token of it can be admitted.
+        int32_t cached = 0;
+        if (cb_alloc_add_seq_cached(A, r.id, r.tokens.data(), r.prompt, &cached) != CB_OK) continue;
+        r.done = cached;
+        if (admit(r, fit_chunk(r))) {
+          out->num_cached += cached;
+        } else {
+          cb_alloc_free_seq(A, r.id);
+          r.done = 0;
+        }
       } else {
         admit(r, fit_chunk(r));
       }

@@ -21,7 +21,8 @@ _POLICIES = {"fifo": 0, "prefill_first": 1}
 class _Batch(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
                 ("num_cow", ctypes.c_int32), ("num_decode", ctypes.c_int32),
-                ("num_finished", ctypes.c_int32), ("cap_seqs", ctypes.c_int32),
+                ("num_finished", ctypes.c_int32), ("num_cached", ctypes.c_int32),
+                ("cap_seqs", ctypes.c_int32),
                 ("cap_cow", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("seq_ids", _I32P), ("cu_seqlens_q", _I32P), ("kv_lens", _I32P),
                 ("block_table", _I32P), ("cow_src", _I32P), ("cow_dst", _I32P)]
@@ -66,6 +67,16 @@ def _lib() -> ctypes.CDLL:
         lib.cb_sched_destroy.argtypes = [P]
         lib.cb_sched_add_request.restype = ctypes.c_int
         lib.cb_sched_add_request.argtypes = [P, I, I, I]
+        lib.cb_alloc_set_prefix_caching.restype = ctypes.c_int
+        lib.cb_alloc_set_prefix_caching.argtypes = [P, I]
+        lib.cb_alloc_add_seq_cached.restype = ctypes.c_int
+        lib.cb_alloc_add_seq_cached.argtypes = [P, I, _I32P, I, _I32P]
+        lib.cb_alloc_hash_blocks.restype = ctypes.c_int
+        lib.cb_alloc_hash_blocks.argtypes = [P, I, _I32P, I]
+        lib.cb_alloc_num_cached.restype = I
+        lib.cb_alloc_num_cached.argtypes = [P]
+        lib.cb_sched_add_request_tokens.restype = ctypes.c_int
+        lib.cb_sched_add_request_tokens.argtypes = [P, I, _I32P, I, I]
         lib.cb_sched_fork_request.restype = ctypes.c_int
         lib.cb_sched_fork_request.argtypes = [P, I, I, I]
         lib.cb_sched_step.restype = ctypes.c_int
@@ -118,6 +129,23 @@ class BlockAllocator:
     def free_seq(self, seq: int) -> None:
         _check(_lib().cb_alloc_free_seq(self._h, seq), "cb_alloc_free_seq")
 
+    def set_prefix_caching(self, enable: bool = True) -> None:
+        _check(_lib().cb_alloc_set_prefix_caching(self._h, int(enable)), "cb_alloc_set_prefix_caching")
+
+    def add_seq_cached(self, seq: int, tokens) -> int:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(_lib().cb_alloc_add_seq_cached(self._h, seq, _ptr(t), t.size, ctypes.byref(n)),
+               "cb_alloc_add_seq_cached")
+        return n.value
+
+    def hash_blocks(self, seq: int, tokens) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(_lib().cb_alloc_hash_blocks(self._h, seq, _ptr(t), t.size), "cb_alloc_hash_blocks")
+
+    def num_cached(self) -> int:
+        return int(_lib().cb_alloc_num_cached(self._h))
+
     def num_free(self) -> int:
         return int(_lib().cb_alloc_num_free(self._h))
 
@@ -149,7 +177,7 @@ class Scheduler:
         self._table = np.empty((cap, alloc.max_blocks), dtype=np.int32)
         self._src = np.empty(cap, dtype=np.int32)
         self._dst = np.empty(cap, dtype=np.int32)
-        self._batch = _Batch(0, 0, 0, 0, 0, cap, cap, alloc.max_blocks, _ptr(self._seq_ids),
+        self._batch = _Batch(0, 0, 0, 0, 0, 0, cap, cap, alloc.max_blocks, _ptr(self._seq_ids),
                              _ptr(self._cu), _ptr(self._kv), _ptr(self._table), _ptr(self._src),
                              _ptr(self._dst))
 
@@ -161,6 +189,11 @@ class Scheduler:
     def add_request(self, rid: int, prompt_len: int, max_new_tokens: int) -> None:
         _check(_lib().cb_sched_add_request(self._h, rid, prompt_len, max_new_tokens),
                "cb_sched_add_request")
+
+    def add_request_tokens(self, rid: int, tokens, max_new_tokens: int) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(_lib().cb_sched_add_request_tokens(self._h, rid, _ptr(t), t.size, max_new_tokens),
+               "cb_sched_add_request_tokens")
 
     def fork_request(self, parent: int, child: int, max_new_tokens: int) -> None:
         _check(_lib().cb_sched_fork_request(self._h, parent, child, max_new_tokens),
@@ -178,4 +211,4 @@ class Scheduler:
                 "kv_lens": self._kv[:s], "block_table": self._table[:s],
                 "cow_src": self._src[:c], "cow_dst": self._dst[:c],
                 "num_tokens": b.num_tokens, "num_decode": b.num_decode,
-                "num_finished": b.num_finished}
+                "num_finished": b.num_finished, "num_cached": b.num_cached}

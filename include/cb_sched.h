@@ -66,6 +66,34 @@ cb_status cb_alloc_append(cb_alloc* a, int32_t seq, int32_t n_tokens, int32_t* c
  * seq it would create with cb_alloc_add_seq: then ceil(n_tokens / block_size)). */
 int32_t cb_alloc_blocks_needed(const cb_alloc* a, int32_t seq, int32_t n_tokens);
 
+/*
+ * Prefix caching (transformers "Continuous batching architecture", sections "Prefix caching"
+ * and "Eviction"; "LLM learning path 3.3", section "Prefix caching and RadixAttention",
+ * hash-based blocks): each completed block of prompt tokens is identified by a 64-bit content
+ * hash chained with the hash of every block before it (FNV-1a over the parent hash's 8 bytes
+ * and the block's token ids, 4 bytes each, little-endian); a later prompt reuses the longest
+ * chain of matching blocks (verified token by token) and skips their prefill.  A freed block
+ * keeps its content and hash; it is reused by a match, or, once no block without cached
+ * content is left, the most recently initialized free block is demoted (its hash dropped) and
+ * handed out.  Off by default; switch it on before the first sequence.
+ */
+cb_status cb_alloc_set_prefix_caching(cb_alloc* a, int32_t enable);
+
+/* A new sequence `seq` whose prompt has n_tokens (>= 1) token ids: it starts with the longest
+ * cached chain of full blocks matching the prompt, at most (n_tokens - 1) / block_size blocks
+ * so that at least the last prompt token is computed; *n_cached = the tokens it holds (a
+ * multiple of block_size; 0 without a match or with caching off). */
+cb_status cb_alloc_add_seq_cached(cb_alloc* a, int32_t seq, const int32_t* tokens,
+                                  int32_t n_tokens, int32_t* n_cached);
+
+/* Register the content hashes of seq's full blocks within its first n_tokens positions, whose
+ * token ids are tokens[0 .. n_tokens) (n_tokens <= the tokens seq holds).  A block whose
+ * content is already cached in another block stays unregistered. */
+cb_status cb_alloc_hash_blocks(cb_alloc* a, int32_t seq, const int32_t* tokens, int32_t n_tokens);
+
+/* Blocks with cached content (in use or free). */
+int32_t cb_alloc_num_cached(const cb_alloc* a);
+
 /* `child` shares every block of `parent` (each count + 1) and its length. */
 cb_status cb_alloc_fork(cb_alloc* a, int32_t parent, int32_t child);
 
@@ -103,6 +131,12 @@ void cb_sched_destroy(cb_sched* s);
 cb_status cb_sched_add_request(cb_sched* s, int32_t id, int32_t prompt_len,
                                int32_t max_new_tokens);
 
+/* As cb_sched_add_request, with the prompt's token ids (copied): with prefix caching on in
+ * the allocator, the request's first admission reuses the cached blocks of its longest cached
+ * prompt prefix and prefills only the rest, and its completed prompt blocks are cached. */
+cb_status cb_sched_add_request_tokens(cb_sched* s, int32_t id, const int32_t* tokens,
+                                      int32_t prompt_len, int32_t max_new_tokens);
+
 /* Parallel sampling: a new request `child` that continues from `parent` (which must be
  * decoding: its prompt done) with the same tokens so far, sharing all of parent's blocks
  * (cb_alloc_fork), and produces max_new_tokens in all counting the ones parent has produced.
@@ -124,6 +158,7 @@ typedef struct {
   int32_t num_seqs, num_tokens, num_cow;
   int32_t num_decode;    /* sequences with q_len == 1 that are decoding */
   int32_t num_finished;  /* requests retired at the start of this step */
+  int32_t num_cached;    /* prompt tokens reused from the prefix cache by this step's admissions */
   int32_t cap_seqs, cap_cow, max_blocks;
   int32_t* seq_ids;
   int32_t* cu_seqlens_q;

@@ -23,6 +23,14 @@ Sources, by page title and section:
     Its "Chunked prefill" paragraph: a prompt that exceeds the remaining budget is processed
     as far as it fits and continued on later steps.
 
+  * transformers "Continuous batching architecture", sections "Prefix caching" and "Eviction",
+    and "LLM learning path 3.3", section "Prefix caching and RadixAttention" (hash-based
+    blocks): a completed block is identified by a hash of its tokens together with the hash of
+    every block before it; a new prompt reuses its longest run of leading cached blocks and
+    skips their prefill; shared blocks are reference-counted; a freed block keeps its content
+    and hash, and when blocks without content run out the most recently initialized one is
+    demoted (hash dropped) and reused.
+
 Readings where the pages leave a step open (each also listed in the design notes):
   * Multi-token growth (a prefill chunk) follows the one-token rule token by token, so at
     most its first token can trigger a copy.
@@ -35,6 +43,12 @@ Readings where the pages leave a step open (each also listed in the design notes
     freed) at the start of the step after its last token.
   * A request admitted in a step is not admitted twice in that step (a prompt completed in the
     step decodes from the next one).
+  * Prefix caching: the hash is 64-bit FNV-1a over the parent hash (8 bytes) and the block's
+    token ids (4 bytes each, little-endian); a match is confirmed by comparing the tokens;
+    only blocks made entirely of prompt tokens are cached (generated tokens have no ids here);
+    a match leaves at least the last prompt token to compute; a block whose content is already
+    cached elsewhere is not registered again; "initialized" = the time the block's hash was
+    registered.
 """
 from __future__ import annotations
 
@@ -47,25 +61,110 @@ def blocks_for(n_tokens: int, bs: int) -> int:
     return -(-n_tokens // bs)
 
 
-class BlockAllocator:
-    """Free list (take from the end), reference counts, block tables and token counts."""
+FNV_OFFSET, FNV_PRIME, MASK64 = 0xCBF29CE484222325, 0x100000001B3, (1 << 64) - 1
 
-    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+
+def fnv1a64(data: bytes) -> int:
+    """64-bit FNV-1a (Fowler, Noll, Vo): for each byte, xor it in, then multiply by the prime."""
+    h = FNV_OFFSET
+    for byte in data:
+        h = ((h ^ byte) * FNV_PRIME) & MASK64
+    return h
+
+
+def block_hash(parent: int, tokens) -> int:
+    """Chained content hash: FNV-1a over the parent hash's 8 bytes and each token id's 4 bytes
+    (little-endian)."""
+    return fnv1a64(int(parent).to_bytes(8, "little") + b"".join(
+        (int(t) & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens))
+
+
+class BlockAllocator:
+    """Free list (take from the end), reference counts, block tables and token counts; with
+    prefix caching, content hashes of full prompt blocks and the initialized free blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int,
+                 prefix_caching: bool = False):
         if num_blocks < 1 or block_size < 4 or max_blocks_per_seq < 1:
             raise AllocatorError("bad pool shape")
         self.bs = block_size
         self.max_blocks = max_blocks_per_seq
-        self.free = list(range(num_blocks))
+        self.free = list(range(num_blocks))      # blocks without cached content
         self.ref = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
+        self.prefix = prefix_caching
+        self.hash_of: dict[int, int] = {}        # block -> content hash
+        self.content: dict[int, tuple] = {}      # block -> (parent hash, token ids)
+        self.born: dict[int, int] = {}           # block -> initialization order
+        self.cache: dict[int, int] = {}          # content hash -> block
+        self.idle: set[int] = set()              # free blocks that keep cached content
+        self.clock = 0
+        self.hashed: dict[int, tuple] = {}       # seq -> (blocks hashed, chain hash)
+
+    def num_free(self) -> int:
+        return len(self.free) + len(self.idle)
 
     def _take(self) -> int:
-        if not self.free:
+        if self.free:
+            b = self.free.pop()
+        elif self.idle:
+            b = max(self.idle, key=lambda x: self.born[x])   # most recently initialized
+            self.idle.discard(b)
+            h = self.hash_of.pop(b)
+            if self.cache.get(h) == b:
+                del self.cache[h]
+            del self.content[b], self.born[b]
+        else:
             raise AllocatorError("out of blocks")
-        b = self.free.pop()
         self.ref[b] = 1
         return b
+
+    def _release(self, b: int) -> None:
+        if self.prefix and b in self.hash_of:
+            self.idle.add(b)
+        else:
+            self.free.append(b)
+
+    def add_seq_cached(self, seq: int, tokens) -> int:
+        """New sequence starting from the longest cached chain of the prompt's full blocks."""
+        if seq in self.tables or len(tokens) < 1:
+            raise AllocatorError("bad sequence")
+        table, chain = [], 0
+        if self.prefix:
+            for j in range(min((len(tokens) - 1) // self.bs, self.max_blocks)):
+                blk = tuple(int(t) for t in tokens[j * self.bs:(j + 1) * self.bs])
+                h = block_hash(chain, blk)
+                b = self.cache.get(h)
+                if b is None or self.content[b] != (chain, blk):
+                    break
+                if self.ref[b] == 0:
+                    self.idle.discard(b)
+                self.ref[b] += 1
+                table.append(b)
+                chain = h
+        self.tables[seq] = table
+        self.lens[seq] = len(table) * self.bs
+        self.hashed[seq] = (len(table), chain)
+        return self.lens[seq]
+
+    def hash_blocks(self, seq: int, tokens, n_tokens: int) -> None:
+        if not self.prefix:
+            return
+        done, chain = self.hashed.get(seq, (0, 0))
+        for j in range(done, n_tokens // self.bs):
+            b = self.tables[seq][j]
+            blk = tuple(int(t) for t in tokens[j * self.bs:(j + 1) * self.bs])
+            h = block_hash(chain, blk)
+            if b not in self.hash_of and self.ref[b] == 1 and h not in self.cache:
+                self.hash_of[b] = h
+                self.content[b] = (chain, blk)
+                self.clock += 1
+                self.born[b] = self.clock
+                self.cache[h] = b
+            chain = h
+            done = j + 1
+        self.hashed[seq] = (done, chain)
 
     def needed(self, seq: int, n: int) -> int:
         """Blocks growing `seq` (or creating it) by n tokens would take from the free list."""
@@ -85,7 +184,7 @@ class BlockAllocator:
         if seq in self.tables:
             raise AllocatorError("sequence exists")
         nb = blocks_for(n_tokens, self.bs)
-        if nb > self.max_blocks or nb > len(self.free):
+        if nb > self.max_blocks or nb > self.num_free():
             raise AllocatorError("does not fit")
         self.tables[seq] = [self._take() for _ in range(nb)]
         self.lens[seq] = n_tokens
@@ -96,7 +195,7 @@ class BlockAllocator:
             raise AllocatorError("no such sequence")
         if blocks_for(self.lens[seq] + n_tokens, self.bs) > self.max_blocks:
             raise AllocatorError("table too narrow")
-        if self.needed(seq, n_tokens) > len(self.free):
+        if self.needed(seq, n_tokens) > self.num_free():
             raise AllocatorError("does not fit")
         copies = []
         table = self.tables[seq]
@@ -117,6 +216,7 @@ class BlockAllocator:
             raise AllocatorError("bad fork")
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
+        self.hashed[child] = self.hashed.get(parent, (0, 0))
         for b in self.tables[child]:
             self.ref[b] += 1
 
@@ -124,12 +224,13 @@ class BlockAllocator:
         for b in self.tables.pop(seq):
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                self._release(b)
         del self.lens[seq]
+        self.hashed.pop(seq, None)
 
     def fits(self, seq: int) -> int:
         """Most tokens seq (or a new sequence) can grow by with the free blocks and table width."""
-        free = len(self.free)
+        free = self.num_free()
         if seq not in self.tables:
             return min(free, self.max_blocks) * self.bs
         table, length = self.tables[seq], self.lens[seq]
@@ -145,8 +246,9 @@ WAITING, PREFILL, DECODE, DONE = "waiting", "prefill", "decode", "done"
 
 
 class Request:
-    def __init__(self, rid: int, prompt: int, max_new: int):
+    def __init__(self, rid: int, prompt: int, max_new: int, tokens=None):
         self.id, self.prompt, self.max_new = rid, prompt, max_new
+        self.tokens = None if tokens is None else [int(t) for t in tokens]
         self.done = 0          # prompt tokens in the cache
         self.generated = 0     # tokens produced
         self.state = WAITING
@@ -165,12 +267,12 @@ class Scheduler:
         self.policy = policy
         self.requests: list[Request] = []   # arrival order; forks join at the end
 
-    def add_request(self, rid: int, prompt: int, max_new: int) -> None:
+    def add_request(self, rid: int, prompt: int, max_new: int, tokens=None) -> None:
         if any(r.id == rid for r in self.requests) or prompt < 1 or max_new < 1:
             raise AllocatorError("bad request")
         if blocks_for(prompt + max_new - 1, self.alloc.bs) > self.alloc.max_blocks:
             raise AllocatorError("request longer than a block table")
-        self.requests.append(Request(rid, prompt, max_new))
+        self.requests.append(Request(rid, prompt, max_new, tokens))
 
     def fork_request(self, parent: int, child: int, max_new: int) -> None:
         p = next(r for r in self.requests if r.id == parent)
@@ -191,13 +293,13 @@ class Scheduler:
                 r.state = DONE
                 finished += 1
         batch = {"seq_ids": [], "q_lens": [], "kv_lens": [], "tables": [], "copies": [],
-                 "num_decode": 0, "finished": finished}
+                 "num_decode": 0, "finished": finished, "cached": 0}
         budget = self.max_tokens
         start_state = {r.id: r.state for r in self.requests}
 
         def admit(r: Request, n: int) -> None:
             nonlocal budget
-            if r.state == WAITING:
+            if r.id not in self.alloc.tables:
                 self.alloc.add_seq(r.id, n)
             else:
                 batch["copies"] += self.alloc.append(r.id, n)
@@ -212,6 +314,8 @@ class Scheduler:
             else:
                 r.done += n
                 r.state = PREFILL
+                if self.alloc.prefix and r.tokens is not None:
+                    self.alloc.hash_blocks(r.id, r.tokens, r.done)
                 if r.done == r.prompt:
                     r.state = DECODE
                     r.generated = 1
@@ -223,8 +327,18 @@ class Scheduler:
                 if start_state[r.id] != kind or r.state != kind:
                     continue
                 if kind == DECODE:
-                    if self.alloc.needed(r.id, 1) <= len(self.alloc.free):
+                    if self.alloc.needed(r.id, 1) <= self.alloc.num_free():
                         admit(r, 1)
+                elif kind == WAITING and self.alloc.prefix and r.tokens is not None:
+                    cached = self.alloc.add_seq_cached(r.id, r.tokens)
+                    r.done = cached
+                    n = min(r.prompt - r.done, budget, self.alloc.fits(r.id))
+                    if n > 0:
+                        batch["cached"] += cached
+                        admit(r, n)
+                    else:
+                        self.alloc.free_seq(r.id)
+                        r.done = 0
                 else:
                     n = min(r.prompt - r.done, budget, self.alloc.fits(r.id))
                     if n > 0:

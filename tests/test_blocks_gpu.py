@@ -126,3 +126,82 @@ def test_scheduler_driven_steps_match_oracle(cuda_lib, policy):
                     pass   # parent already at its last token
     assert copies > 0
     assert np.array_equal(bits_of(kp), k_or) and np.array_equal(bits_of(vp), v_or)
+
+
+def _rows(seed, shape):
+    rng = np.random.default_rng(seed)
+    return workloads.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+
+def _prefix_run(prefix, requests, P, bs, Hq, Hkv, D, MB):
+    """Run `requests` (id, tokens, new) through the native scheduler and the GPU path; every
+    token's q/k/v rows are a function of its request's token prefix (prompt positions) or of
+    (request, position) (generated positions), as a model's would be.  Returns the output row
+    of every computed (request, position) and checks each step against the oracle."""
+    alloc = BlockAllocator(P, bs, MB)
+    alloc.set_prefix_caching(prefix)
+    sched = Scheduler(alloc, max_batch_tokens=80, max_requests_per_batch=6)
+    seeds = {}
+    for rid, toks, new in requests:
+        sched.add_request_tokens(rid, toks, new)
+        h, hs = 0, []
+        for t in toks:
+            h = (h * 1000003 + t + 1) % (1 << 61)
+            hs.append(h)
+        seeds[rid] = hs
+    k_or = np.zeros((P, bs, Hkv, D), dtype=np.uint16)
+    v_or = np.zeros_like(k_or)
+    kp, vp = bf16_tensor(k_or), bf16_tensor(v_or)
+    scale = 1.0 / np.sqrt(D)
+    outs, cached, steps = {}, 0, 0
+    while sched.num_active():
+        st = sched.step()
+        steps += 1
+        assert steps < 400
+        cached += st["num_cached"]
+        S = len(st["seq_ids"])
+        if S == 0:
+            continue
+        cu, kvl, table = (st["cu_seqlens_q"].copy(), st["kv_lens"].copy(),
+                          st["block_table"].copy())
+        qs, ks, vs, keys = [], [], [], []
+        for i, rid in enumerate(st["seq_ids"].tolist()):
+            n = int(cu[i + 1] - cu[i])
+            for p in range(int(kvl[i]) - n, int(kvl[i])):
+                hs = seeds[rid]
+                sd = hs[p] if p < len(hs) else (rid * 1000003 + p) * 7 + 5
+                qs.append(_rows(sd * 3 + 0, (Hq, D)))
+                ks.append(_rows(sd * 3 + 1, (Hkv, D)))
+                vs.append(_rows(sd * 3 + 2, (Hkv, D)))
+                keys.append((rid, p))
+        q, kn, vn = np.stack(qs), np.stack(ks), np.stack(vs)
+        cb.kv_append(bf16_tensor(kn), bf16_tensor(vn), kp, vp, i32(table), i32(cu), i32(kvl), bs)
+        out = cb.ragged_paged_attention(bf16_tensor(q), kp, vp, i32(table), i32(cu), i32(kvl),
+                                        bs, scale).float().cpu().numpy()
+        assert cb.get_device_error() == cb.CB_OK
+        k_or, v_or = opa.kv_append(kn, vn, k_or, v_or, table, cu, kvl, bs)
+        ref, _ = opa.ragged_paged_attention(q, k_or, v_or, table, cu, kvl, bs, scale)
+        assert_close(out, ref, f"prefix={prefix} step {steps}")
+        for j, key in enumerate(keys):
+            outs[key] = out[j]
+    return outs, cached
+
+
+def test_prefix_cache_gives_the_outputs_of_a_full_prefill(cuda_lib):
+    # requests sharing system prompts: with the prefix cache on, later requests skip the
+    # cached blocks' prefill, and every row they do compute equals the row computed with the
+    # cache off (each position's K/V is a function of its token prefix, as a model's would be)
+    rng = random.Random(23)
+    systems = [[rng.randrange(30000) for _ in range(n)] for n in (150, 90)]
+    requests = []
+    for rid in range(10):
+        sysp = systems[rid % 2][:rng.randint(40, 150)]
+        toks = sysp + [rng.randrange(30000) for _ in range(rng.randint(1, 40))]
+        requests.append((rid, toks, rng.randint(1, 6)))
+    P, bs, Hq, Hkv, D, MB = 200, 16, 8, 2, 64, 16
+    full, c0 = _prefix_run(False, requests, P, bs, Hq, Hkv, D, MB)
+    hit, c1 = _prefix_run(True, requests, P, bs, Hq, Hkv, D, MB)
+    assert c0 == 0 and c1 > 0
+    assert set(hit) <= set(full) and len(hit) < len(full)
+    for key, row in hit.items():
+        assert_close(row, full[key].astype(np.float64), f"row {key}", atol=4e-2, rtol=2e-2)

@@ -18,7 +18,8 @@ import random
 
 import pytest
 
-from oracle.scheduler import AllocatorError, BlockAllocator, Scheduler, blocks_for
+from oracle.scheduler import (AllocatorError, BlockAllocator, Scheduler, block_hash, blocks_for,
+                              fnv1a64)
 
 
 def test_allocator_fork_copy_on_write_example():
@@ -199,3 +200,91 @@ def test_continuous_is_list_scheduling_and_beats_static():
 
 def test_blocks_for_matches_the_printed_examples():
     assert blocks_for(1000, 16) == 63 and blocks_for(8192, 256) == 32
+
+
+# ------------------------------------------------------------------------------ prefix caching
+
+def test_fnv1a64_published_vectors():
+    # the FNV authors' test vectors for 64-bit FNV-1a
+    assert fnv1a64(b"") == 0xCBF29CE484222325
+    assert fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_block_hash_chains_the_prefix():
+    a, b = [1, 2, 3, 4], [5, 6, 7, 8]
+    assert block_hash(0, a) != block_hash(0, b)
+    assert block_hash(block_hash(0, a), b) != block_hash(block_hash(0, b), b)  # same block, other prefix
+    assert block_hash(7, a) == fnv1a64((7).to_bytes(8, "little") + bytes([1, 0, 0, 0, 2, 0, 0, 0,
+                                                                         3, 0, 0, 0, 4, 0, 0, 0]))
+
+
+def _prefix_sched(num_blocks=400, bs=16, budget=4096, cap=8):
+    return Scheduler(BlockAllocator(num_blocks, bs, 200, prefix_caching=True), budget, cap)
+
+
+def test_shared_system_prompt_skips_its_prefill():
+    # the page's example: a 1,000-token system prompt S shared by three requests; the first
+    # misses, the later ones skip ~1,000 tokens of prefill (whole blocks of S here)
+    rng = random.Random(3)
+    S = [rng.randrange(50000) for _ in range(1000)]
+    r1 = S + [11, 12, 13, 14]
+    r2 = S + [11, 12, 15]
+    r3 = S + [rng.randrange(50000) for _ in range(200)]
+    s = _prefix_sched()
+    s.add_request(1, len(r1), 2, r1)
+    b = s.step()
+    assert b["q_lens"] == [1004] and b["cached"] == 0
+    s.add_request(2, len(r2), 2, r2)
+    s.add_request(3, len(r3), 2, r3)
+    b = s.step()
+    prefill = dict(zip(b["seq_ids"], b["q_lens"]))
+    assert b["cached"] == 2 * 992                      # 62 full blocks of S each
+    assert prefill[2] == len(r2) - 992 and prefill[3] == len(r3) - 992
+    t1 = s.alloc.tables[1]
+    assert s.alloc.tables[2][:62] == t1[:62] == s.alloc.tables[3][:62]
+    assert all(s.alloc.ref[x] == 3 for x in t1[:62])
+
+
+def test_a_match_leaves_the_last_token_to_compute():
+    toks = list(range(64))                             # exactly 4 blocks of 16
+    s = _prefix_sched()
+    s.add_request(1, 64, 1, toks)
+    s.step()
+    s.add_request(2, 64, 1, toks)
+    b = s.step()
+    assert b["seq_ids"] == [2] and b["q_lens"] == [16] and b["cached"] == 48
+
+
+def test_cached_blocks_outlive_their_requests_and_are_reused():
+    toks = list(range(100, 164))
+    s = _prefix_sched()
+    s.add_request(1, 64, 1, toks)
+    s.step()
+    s.step()                                           # retires request 1
+    assert not s.alloc.tables and s.alloc.num_free() == 400
+    assert len(s.alloc.idle) == 4                      # its 4 prompt blocks keep their content
+    s.add_request(2, 64 + 5, 1, toks + [1, 2, 3, 4, 5])
+    b = s.step()
+    assert b["cached"] == 64 and b["q_lens"] == [5]
+
+
+def test_eviction_demotes_the_most_recently_initialized_block_first():
+    s = _prefix_sched(num_blocks=6, bs=4, cap=4)
+    a_toks, b_toks = [1] * 8 + [9], [2] * 8 + [9]      # 2 cacheable blocks + 1 partial each
+    s.add_request(1, 9, 1, a_toks)
+    s.step()
+    s.add_request(2, 9, 1, b_toks)
+    s.step()                                           # retires 1, prefills 2
+    s.step()                                           # retires 2
+    al = s.alloc
+    order = sorted(al.idle, key=lambda x: al.born[x])
+    assert len(order) == 4 and al.num_free() == 6
+    # 2 blocks without content left; a 16-token sequence needs 4: the two most recently
+    # initialized cached blocks (request 2's) are demoted first
+    al.add_seq(99, 16)
+    assert set(al.tables[99]) >= set(order[2:])
+    assert set(order[:2]) <= al.idle                   # request 1's prefix is still cached
+    al.free_seq(99)
+    s.add_request(3, 9, 1, a_toks)
+    assert s.step()["cached"] == 8

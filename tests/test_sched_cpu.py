@@ -28,28 +28,43 @@ def _same_step(nb, ob, max_blocks):
 
 
 def _drive(seed, policy, num_blocks, bs, max_blocks, budget, cap, n_req, fork_p=0.0,
-           arrive_every=3):
+           arrive_every=3, prefix=False):
     rng = random.Random(seed)
     na = BlockAllocator(num_blocks, bs, max_blocks)
+    if prefix:
+        na.set_prefix_caching(True)
     ns = Scheduler(na, budget, cap, policy)
-    oa = osch.BlockAllocator(num_blocks, bs, max_blocks)
+    oa = osch.BlockAllocator(num_blocks, bs, max_blocks, prefix_caching=prefix)
     os_ = osch.Scheduler(oa, budget, cap, policy)
+    systems = [[rng.randrange(1000) for _ in range(rng.randint(1, 300))] for _ in range(4)]
     pending = []
     for r in range(n_req):
         limit = max_blocks * bs
-        p = rng.randint(1, min(600, limit - 1))
+        if prefix:
+            # a shared system prompt (or part of one) and a private suffix
+            sysp = rng.choice(systems)[:rng.randint(0, 300)]
+            toks = sysp + [rng.randrange(1000) for _ in range(rng.randint(1, 200))]
+            toks = toks[:limit - 1]
+            p = len(toks)
+        else:
+            toks = None
+            p = rng.randint(1, min(600, limit - 1))
         n = rng.randint(1, min(60, limit - p + 1))
-        pending.append((r, p, n))
+        pending.append((r, p, n, toks))
     next_id = n_req
     steps = 0
+    cached_total = [0]
     while pending or os_.num_active():
         # a few arrivals every `arrive_every` steps
         if pending and steps % arrive_every == 0:
             for _ in range(rng.randint(1, 4)):
                 if pending:
-                    r, p, n = pending.pop(0)
-                    ns.add_request(r, p, n)
-                    os_.add_request(r, p, n)
+                    r, p, n, toks = pending.pop(0)
+                    if toks is None:
+                        ns.add_request(r, p, n)
+                    else:
+                        ns.add_request_tokens(r, toks, n)
+                    os_.add_request(r, p, n, toks)
         # parallel sampling: fork a decoding request now and then
         if fork_p and rng.random() < fork_p:
             dec = [q for q in os_.requests if q.state == osch.DECODE and q.generated < q.max_new]
@@ -62,13 +77,18 @@ def _drive(seed, policy, num_blocks, bs, max_blocks, budget, cap, n_req, fork_p=
                 next_id += 1
         nb, ob = ns.step(), os_.step()
         _same_step(nb, ob, max_blocks)
-        assert na.num_free() == len(oa.free)
+        assert nb["num_cached"] == ob["cached"]
+        cached_total[0] += ob["cached"]
+        assert na.num_free() == oa.num_free()
+        assert na.num_cached() == len(oa.cache)
         assert [na.ref_count(b) for b in range(num_blocks)] == oa.ref
         steps += 1
         assert steps < 20000
         if not ob["seq_ids"] and not pending and os_.num_active():
             break  # stalled on the cache budget (no preemption): both must agree on that too
     assert ns.num_active() == os_.num_active()
+    if prefix:
+        assert cached_total[0] > 0
     return steps
 
 
@@ -88,6 +108,15 @@ def test_native_scheduler_tight_pool(policy):
 def test_native_scheduler_with_forks_and_copy_on_write(policy):
     _drive(21, policy, num_blocks=3000, bs=4, max_blocks=200, budget=300, cap=24, n_req=60,
            fork_p=0.3)
+
+
+@pytest.mark.parametrize("policy", ["fifo", "prefill_first"])
+@pytest.mark.parametrize("num_blocks", [5000, 260])
+def test_native_prefix_cache_matches_oracle(policy, num_blocks):
+    # shared system prompts: cache hits, blocks kept after their requests end, and (small
+    # pool) demotion of the most recently initialized cached blocks
+    _drive(41 + num_blocks, policy, num_blocks=num_blocks, bs=16, max_blocks=40, budget=400,
+           cap=16, n_req=80, prefix=True, fork_p=0.1)
 
 
 def test_native_scheduler_small_cap_large_budget():
