@@ -59,9 +59,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--serial", action="store_true",
                    help="run the chunk kernel after the decode kernel instead of concurrently")
-    p.add_argument("--mode", choices=["path", "blocks", "serve"], default="path",
+    p.add_argument("--mode", choices=["path", "blocks", "serve", "graphs"], default="path",
                    help="path: the attention hot path (default); blocks: KV block copy / "
-                        "offload / restore kernels; serve: a scheduler-driven serving loop")
+                        "offload / restore kernels; serve: a scheduler-driven serving loop; "
+                        "graphs: step latency eager vs CUDA-graph replay")
     p.add_argument("--policy", choices=["fifo", "prefill_first"], default="fifo")
     return p.parse_args()
 
@@ -522,12 +523,77 @@ def run_serve(args, local: int):
     print(json.dumps(line), flush=True)
 
 
+def run_graphs(args, local: int):
+    """Latency of one step (append + attention, from the call to its completion on the GPU)
+    issued eagerly through the Python API vs replayed from a captured CUDA graph, for decode
+    batches of 1, 8 and 64 sequences (kv_len 1024) and the 2048-token mixed batch."""
+    import torch
+    import continuous_batching_paged_gb300 as cb
+    from continuous_batching_paged_gb300.graphs import GraphedStep
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shapes = [("decode x1", [1], [1024]), ("decode x8", [1] * 8, [1024] * 8),
+              ("decode x64", [1] * 64, [1024] * 64), ("mixed 2048", None, None)]
+    rows = []
+    for name, ql, kl in shapes:
+        b = (workloads.make_config(3) if ql is None else
+             workloads.build_batch(ql, kl, 32, 8, 128, 32, seed=77, name=name))
+        t16 = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+        t32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(dev)
+        q, kn, vn = t16(b.q), t16(b.k_new), t16(b.v_new)
+        kp, vp = t16(b.k_pages), t16(b.v_pages)
+        tab, cu, kv = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
+        out = torch.empty_like(q)
+        ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                           b.num_pages, b.max_blocks, b.block_size, b.num_tokens),
+                         dtype=torch.uint8, device=dev)
+
+        def eager():
+            cb.kv_append(kn, vn, kp, vp, tab, cu, kv, b.block_size)
+            cb.ragged_paged_attention(q, kp, vp, tab, cu, kv, b.block_size, b.scale, out=out,
+                                      workspace=ws)
+
+        g = GraphedStep(kp, vp, b.block_size, b.scale, b.num_q_heads, b.max_blocks)
+        g.run(q, kn, vn, tab, cu, kv)                 # capture, inputs into the graph buffers
+        bucket = g.buffers(b.num_seqs, b.num_tokens)
+
+        def graph():
+            g.run(q, kn, vn, tab, cu, kv)
+
+        def replay():
+            g.replay(bucket)
+
+        res = {}
+        for label, fn in (("eager", eager), ("graph", graph), ("replay", replay)):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(max(20, min(args.steps, 200))):
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            res[label] = 1e6 * statistics.median(ts)
+        cb.check_device_error()
+        rows.append({"batch": name, "seqs": b.num_seqs, "tokens": b.num_tokens,
+                     "eager_us": res["eager"], "graph_with_input_copies_us": res["graph"],
+                     "replay_inputs_in_place_us": res["replay"],
+                     "speedup_in_place": res["eager"] / res["replay"]})
+    print(json.dumps({"metric": "step latency (append + attention, call to completion), eager "
+                                "Python API vs CUDA-graph replay", "mode": "graphs", "n_gpus": 1,
+                      "data": "synthetic", "unit": "us (median)", "rows": rows,
+                      "note": "graph_with_input_copies copies the step's inputs into the graph's "
+                              "static buffers first; replay_inputs_in_place is for a producer "
+                              "that writes them there (GraphedStep.buffers)"}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.mode != "path":
         world, rank, local = dist_setup(args)
         if rank == 0:
-            (run_blocks if args.mode == "blocks" else run_serve)(args, local)
+            {"blocks": run_blocks, "serve": run_serve, "graphs": run_graphs}[args.mode](args, local)
         return
     world, rank, local = dist_setup(args)
     cfg = WORKLOADS[args.workload]

@@ -179,7 +179,7 @@ cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void
     return fail(CB_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
     return fail(CB_ERR_INVALID_ARG, "K/V tensors must be 16-byte aligned");
-  if (dims->num_seqs == 0) return fail(CB_ERR_INVALID_ARG, "tokens without sequences");
+  if (dims->num_seqs == 0) return CB_OK;  // every token row is padding
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != CB_OK) return st;
@@ -214,7 +214,7 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   cb_status st = check_dims(dims, block_size);
   if (st != CB_OK) return st;
   if (dims->num_tokens == 0) return CB_OK;
-  if (dims->num_seqs == 0) return fail(CB_ERR_INVALID_ARG, "tokens without sequences");
+  if (dims->num_seqs == 0) return CB_OK;  // every token row is padding
   if (!q || !k_pages || !v_pages || !block_table || !cu_seqlens_q || !kv_lens || !out || !workspace)
     return fail(CB_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))

@@ -26,7 +26,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a)
   uint4* kp = static_cast<uint4*>(a.k_pages);
   uint4* vp = static_cast<uint4*>(a.v_pages);
   const int nwarps = gridDim.x * (kAppendThreads / 32);
-  for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
+  // Rows at or past cu_seqlens_q[S] are padding of the token tensors: left untouched.
+  const int t_end = min(a.T, __ldg(a.cu_seqlens_q + a.S));
+  for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < t_end; t += nwarps) {
     // Sequence of token t: the last s with cu[s] <= t (cu is non-decreasing).  Each round
     // probes 32 increasing positions in (lo, hi]; the lanes whose probe is <= t form a prefix.
     int lo = 0, hi = a.S;
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   const long long max_kv = (long long)a.max_blocks * a.bs;
 
   if (tid == 0) {
-    if (a.cu_seqlens_q[0] != 0 || a.cu_seqlens_q[a.S] != a.T) report(a.err, kErrOutOfRange);
+    if (a.cu_seqlens_q[0] != 0 || a.cu_seqlens_q[a.S] > a.T) report(a.err, kErrOutOfRange);
   }
   __syncthreads();
   float my_keys = 0.f, my_pairs = 0.f;  // work estimates for the decode / chunk balance

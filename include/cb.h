@@ -34,7 +34,11 @@
  *   block_table       int32 [S, MB]           entry j = physical block holding tokens
  *                                             [j*bs, (j+1)*bs) of the sequence; unused
  *                                             entries are never read
- *   cu_seqlens_q      int32 [S+1]             cu[0] = 0, non-decreasing, cu[S] = T
+ *   cu_seqlens_q      int32 [S+1]             cu[0] = 0, non-decreasing, cu[S] <= T; rows
+ *                                             cu[S] .. T-1 of q/out/k_new/v_new are padding
+ *                                             (never read, never written), so a caller can
+ *                                             keep fixed buffer shapes (e.g. in a CUDA graph
+ *                                             captured for a padded shape)
  *   kv_lens           int32 [S]               keys visible to sequence s INCLUDING this
  *                                             step's appended tokens (kv_len >= q_len)
  *   lse               fp32  [T, Hq]           optional natural-log softmax normaliser
@@ -63,7 +67,7 @@ typedef enum {
 
 typedef struct {
   int32_t num_seqs;            /* S  >= 0                                           */
-  int32_t num_tokens;          /* T  >= 0, must equal cu_seqlens_q[S]               */
+  int32_t num_tokens;          /* T  >= cu_seqlens_q[S]: rows of the token tensors  */
   int32_t num_q_heads;         /* Hq >= 1, a multiple of Hkv, Hq / Hkv <= 16        */
   int32_t num_kv_heads;        /* Hkv >= 1                                          */
   int32_t head_dim;            /* D: 64 or 128                                      */
