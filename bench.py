@@ -64,6 +64,8 @@ def parse_args():
                         "offload / restore kernels; serve: a scheduler-driven serving loop; "
                         "graphs: step latency eager vs CUDA-graph replay")
     p.add_argument("--policy", choices=["fifo", "prefill_first"], default="fifo")
+    p.add_argument("--window", type=int, default=0,
+                   help="sliding-window attention over the last W keys (0: full causal)")
     return p.parse_args()
 
 
@@ -79,7 +81,7 @@ def peaks():
 
 # ----------------------------------------------------------------------------- workload facts
 
-def decode_kv_bytes(b: workloads.Batch):
+def decode_kv_bytes(b: workloads.Batch, window: int = 0):
     """Algorithmic HBM bytes of the decode pass: every distinct K/V row a decode token reads
     (shared prefix pages once), plus its q and out rows; and the same with sharing counted per
     sequence ("logical")."""
@@ -90,24 +92,28 @@ def decode_kv_bytes(b: workloads.Batch):
     n_dec = 0
     for s in np.nonzero(q_lens == 1)[0]:
         kv = int(b.kv_lens[s])
-        j = np.arange(kv)
+        j = np.arange(max(0, kv - window) if window > 0 else 0, kv)
         slots.append(b.block_table[s][j // b.block_size].astype(np.int64) * b.block_size
                      + j % b.block_size)
-        logical += kv
+        logical += j.size
         n_dec += 1
     unique = int(np.unique(np.concatenate(slots)).size) if slots else 0
     qo = n_dec * b.num_q_heads * b.head_dim * 2 * 2
     return unique * row_bytes + qo, logical * row_bytes + qo
 
 
-def chunk_flops(b: workloads.Batch):
+def chunk_flops(b: workloads.Batch, window: int = 0):
     """Algorithmic FLOPs of the chunk pass: 4 * D * Hq per unmasked (query, key) pair."""
     q_lens = np.diff(b.cu_seqlens_q)
     pairs = 0
     for s in np.nonzero(q_lens > 1)[0]:
         n = int(q_lens[s])
         ctx = int(b.kv_lens[s]) - n
-        pairs += n * ctx + n * (n + 1) // 2
+        if window > 0:
+            pos = np.arange(ctx, ctx + n) + 1          # keys visible: min(position + 1, W)
+            pairs += int(np.minimum(pos, window).sum())
+        else:
+            pairs += n * ctx + n * (n + 1) // 2
     return 4.0 * b.head_dim * b.num_q_heads * pairs
 
 
@@ -336,7 +342,8 @@ def workload_config(b: workloads.Batch, args):
             "head_dim": b.head_dim, "block_size": b.block_size, "pages": b.num_pages,
             "seed": 1000 + WORKLOADS[args.workload],
             "l2": "flushed before every timed step (512 MiB write, then 512 MiB read); KV also exceeds L2",
-            "parallelism": f"replicas x{args.gpus}"}
+            "parallelism": f"replicas x{args.gpus}",
+            **({"window": args.window} if getattr(args, "window", 0) else {})}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -645,7 +652,8 @@ def main():
         cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
         cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, out=out,
                                   workspace=ws, decode_ctas=args.decode_ctas,
-                                  phase_events=ph if record else None, serial=args.serial)
+                                  phase_events=ph if record else None, serial=args.serial,
+                                  window=args.window)
 
     # correctness guard before timing: the error word must be clear after one step
     step(False)
@@ -771,7 +779,8 @@ def main():
         comp.wait_event(d2h_done[j])               # out buffer j has been read back
         cb.kv_append(bk, bv, kp, vp, btab, bcu, bkv, b.block_size)
         cb.ragged_paged_attention(bq, kp, vp, btab, bcu, bkv, b.block_size, b.scale, out=bo,
-                                  workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial)
+                                  workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial,
+                                  window=args.window)
         comp_done[j].record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[j])
@@ -790,8 +799,8 @@ def main():
     cb.check_device_error()
 
     pk, pk_kind = peaks()
-    dec_bytes, dec_logical = decode_kv_bytes(b)
-    flops = chunk_flops(b)
+    dec_bytes, dec_logical = decode_kv_bytes(b, args.window)
+    flops = chunk_flops(b, args.window)
     dec_ms, chunk_ms = per_kernel["decode"], per_kernel["chunk"]
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 and dec_bytes else None
     chunk_tf = flops / (chunk_ms * 1e-3) / 1e12 if chunk_ms > 0 and flops else None

@@ -51,7 +51,8 @@ OPT_SERIAL = 1
 class CbOptions(ctypes.Structure):
     _fields_ = [("decode_ctas", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("reserved", ctypes.c_int64 * 4)]
+                ("window", ctypes.c_int32), ("reserved32", ctypes.c_int32),
+                ("reserved", ctypes.c_int64 * 3)]
 
 
 class CbError(RuntimeError):
@@ -247,14 +248,16 @@ def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max
 
 def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size,
                            scale, out=None, lse=None, workspace=None, decode_ctas: int = 0,
-                           phase_events=None, serial: bool = False, stream=None):
+                           phase_events=None, serial: bool = False, window: int = 0,
+                           stream=None):
     """One attention pass over the ragged batch (cb_ragged_paged_attention_ex).
 
     q [T, Hq, D] bf16; pages [P, bs, Hkv, D] bf16 (after the append); returns out [T, Hq, D]
     bf16, or (out, lse) when ``lse`` is True or an fp32 [T, Hq] tensor.  ``phase_events``:
     optional sequence of NUM_PHASE_EVENTS recorded torch.cuda.Event objects; the call records
     them around its planner, decode and chunk kernels (see cb_options in cb.h).  ``serial``
-    runs the chunk kernel after the decode kernel instead of concurrently.
+    runs the chunk kernel after the decode kernel instead of concurrently.  ``window`` > 0
+    selects sliding-window attention over the last ``window`` keys of each query.
     """
     import torch
     _check_bf16("q", q, 3)
@@ -283,6 +286,7 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _require(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be uint8")
     opts = CbOptions(int(decode_ctas), OPT_SERIAL if serial else 0)
+    opts.window = int(window)
     if phase_events is not None:
         _require(len(phase_events) == NUM_PHASE_EVENTS, f"need {NUM_PHASE_EVENTS} phase events")
         handles = (ctypes.c_void_p * NUM_PHASE_EVENTS)(*[int(e.cuda_event) for e in phase_events])

@@ -262,6 +262,8 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
   if (dctas > CB_MAX_DECODE_CTAS) dctas = CB_MAX_DECODE_CTAS;
   a.decode_ctas = dctas;
   a.prefill_ctas = ds->sm_count;
+  a.window = options != nullptr ? options->window : 0;
+  if (a.window < 0) return fail(CB_ERR_INVALID_ARG, "window must be >= 0, got %d", a.window);
   a.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap qmap, kmap, vmap, kmap_c, vmap_c;

@@ -205,8 +205,10 @@ __device__ int pf_unit_bin(const AttnArgs& a, const int32_t* pf_seq, const int32
   const int s = pf_seq[lo];
   const int u = g - pf_prefix[lo];
   const int q_len = a.cu_seqlens_q[s + 1] - a.cu_seqlens_q[s];
+  const int ctx = a.kv_lens[s] - q_len;
   const int rows = min((u + 1) * pf_unit_tiles(a.G) * kPrefillTileM, q_len);
-  const int tiles = (a.kv_lens[s] - q_len + rows + kChunkKeys - 1) / kChunkKeys;
+  const int first = window_first_key(ctx + u * pf_unit_tiles(a.G) * kPrefillTileM, a.window);
+  const int tiles = (ctx + rows + kChunkKeys - 1) / kChunkKeys - first / kChunkKeys;
   return kCostBins - 1 - min(tiles, kCostBins - 1);
 }
 
@@ -249,12 +251,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
         report(a.err, kErrOutOfRange);
         bad = true;
       } else if (q_len == 1) {
+        // tiles from the one holding the window's first key (every key without a window)
+        const int first = window_first_key(kv - 1, a.window) / kDecodeTileKeys * kDecodeTileKeys;
         v[0] = 1;
-        v[1] = (kv + kDecodeTileKeys - 1) / kDecodeTileKeys;
-        my_keys += (float)kv;
+        v[1] = (kv - first + kDecodeTileKeys - 1) / kDecodeTileKeys;
+        my_keys += (float)(kv - window_first_key(kv - 1, a.window));
       } else if (q_len > 1) {
         v[2] = 1;
-        my_pairs += (float)q_len * (float)(kv - q_len) + 0.5f * (float)q_len * (float)(q_len + 1);
+        if (a.window > 0) {  // sum over the chunk's rows of min(position + 1, window)
+          const float W = (float)a.window;
+          for (int i = 0; i < q_len; i += 64) {
+            const int i1 = min(i + 64, q_len);
+            const float p0 = (float)(kv - q_len + i + 1), p1 = (float)(kv - q_len + i1);
+            my_pairs += (i1 - i) * fminf(0.5f * (p0 + p1), W);
+          }
+        } else {
+          my_pairs += (float)q_len * (float)(kv - q_len) + 0.5f * (float)q_len * (float)(q_len + 1);
+        }
         v[3] = (q_len + unit_rows - 1) / unit_rows;  // work units (pf_unit_tiles)
       }
     }

@@ -32,6 +32,11 @@ __host__ __device__ inline int pf_unit_tiles(int G) { return pf_pair_heads(G) ? 
 
 constexpr int kCostBins = 1024;  // histogram bins of the planner's longest-first unit order
 
+// Sliding window: the first key a query at absolute position p sees (0 without a window).
+__host__ __device__ inline int window_first_key(int p, int window) {
+  return (window > 0 && p >= window) ? p - window + 1 : 0;
+}
+
 // Workspace header (int32 words).
 struct PlanHeader {
   int32_t n_dec;          // number of decode sequences (q_len == 1)

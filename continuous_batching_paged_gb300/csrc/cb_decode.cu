@@ -33,6 +33,7 @@ struct StageInfo {
   int dec;       // index among decode sequences (partial-result slot = cta + dec)
   int tok;       // packed token index of the sequence's query
   int kv;        // kv_len
+  int lo;        // first key in the window (0 without a sliding window)
   int key0;      // first key of this tile
   uint32_t flags;
   int p0, p1;    // the sequence's tile range [p0, p1) in the concatenated tile order
@@ -215,6 +216,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
     const uint32_t kst = sbase + stage * SM::kStageBytes;
     const uint32_t vst = kst + SM::kKVBytes;
     const bool tail = si.key0 + kDecodeTileKeys > si.kv;
+    const bool head = si.key0 < si.lo;  // keys before the sliding window in this tile
 
     // ---- K fragments (A operand of S^T: rows = keys, k = head dim)
     uint32_t kf[KS][4];
@@ -259,8 +261,9 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) mma_bf16_16816(s[ht], kf[ks], qb[ht][ks][0], qb[ht][ks][1]);
     }
-    if (tail) {
-      const bool dead0 = si.key0 + g >= si.kv, dead1 = si.key0 + g + 8 >= si.kv;
+    if (tail || head) {
+      const bool dead0 = si.key0 + g >= si.kv || si.key0 + g < si.lo;
+      const bool dead1 = si.key0 + g + 8 >= si.kv || si.key0 + g + 8 < si.lo;
 #pragma unroll
       for (int ht = 0; ht < NTH; ++ht) {
         if (dead0) s[ht][0] = s[ht][1] = -INFINITY;
@@ -449,6 +452,9 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
       const int s = dec_seq[d];
       const int kv = a.kv_lens[s];
       const int tok = a.cu_seqlens_q[s];
+      // with a sliding window the sequence's tiles start at the one holding its first key
+      const int lo_key = window_first_key(kv - 1, a.window);
+      const int first_tile_key = lo_key / kDecodeTileKeys * kDecodeTileKeys;
       const long long lo = t > p0 ? t : p0;
       const long long hi = t1 < p1 ? t1 : p1;
       const bool complete = p0 >= t0 && p1 <= t1;
@@ -458,7 +464,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
         int entry = -1;
         {
           const long long tile = tb + lane / nsb;
-          const int pos = (int)(tile - p0) * kDecodeTileKeys + (lane % nsb) * KB;
+          const int pos = first_tile_key + (int)(tile - p0) * kDecodeTileKeys + (lane % nsb) * KB;
           if (lane < tiles_per_batch * nsb && tile < hi && pos < kv) {
             const int lb = pos / a.bs;
             entry = lb < a.max_blocks ? __ldg(row + lb) : -2;
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
           }
           abort = __shfl_sync(0xffffffffu, abort, 0);
           if (abort) break;
-          const int key0 = (int)(tile - p0) * kDecodeTileKeys;
+          const int key0 = first_tile_key + (int)(tile - p0) * kDecodeTileKeys;
           // One TMA box per (page run sb, half of D, K or V) covers all HB heads of the run:
           // lane sb handles run sb (nsb <= 16 runs per tile).
           const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (lane < nsb ? lane : 0));
@@ -490,6 +496,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             si.dec = d;
             si.tok = tok;
             si.kv = kv;
+            si.lo = lo_key;
             si.key0 = key0;
             si.p0 = (int)p0;
             si.p1 = (int)p1;

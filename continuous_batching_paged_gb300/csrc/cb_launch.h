@@ -34,6 +34,7 @@ struct AttnArgs {
   int decode_ctas;     // CTAs of the decode pass (<= CB_MAX_DECODE_CTAS)
   int decode_auto;     // 1: the planner picks how many of them work (decode / chunk balance)
   int prefill_ctas;    // persistent CTAs of the prefill pass
+  int window;          // > 0: query at position p sees keys (p - window, p]; 0: all <= p
   float scale_log2;    // softmax scale * log2(e)
 };
 

@@ -72,6 +72,7 @@ struct PfItem {
   int head[2], tok[2], rows[2], nk[2], nt[2];  // per tile: query head, first token, valid rows,
                                                // keys, K/V tiles
   int nt_all, nk_all;                          // K/V tiles loaded and keys covered for the item
+  int j0;                                      // first K/V tile (a sliding window skips older)
   bool hasB;
 };
 
@@ -122,6 +123,8 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
   }
   it.nk_all = max(it.nk[0], it.nk[1]);
   it.nt_all = max(it.nt[0], it.nt[1]);
+  // tile A's first row is the item's earliest query; keys before its window are not needed
+  it.j0 = window_first_key(it.ctx + qt[0] * kPrefillTileM, a.window) / kChunkKeys;
   return it;
 }
 
@@ -218,10 +221,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // Stage the item's block-table entries in shared memory with coalesced loads issued
         // back to back, so the per-tile loop below never waits on a global load.
         int* ecache = reinterpret_cast<int*>(smem + SM::kEntries);
-        const int n_ent = min(min((it.nk_all + a.bs - 1) / a.bs, a.max_blocks), kEntryCache);
-        for (int i = lane; i < n_ent; i += 32) ecache[i] = __ldg(row + i);
+        const int e0 = it.j0 * kChunkKeys / a.bs;  // first block the item reads
+        const int n_ent =
+            max(0, min(min((it.nk_all + a.bs - 1) / a.bs, a.max_blocks) - e0, kEntryCache));
+        for (int i = lane; i < n_ent; i += 32) ecache[i] = __ldg(row + e0 + i);
         __syncwarp();
-        for (int j = 0; j < it.nt_all; ++j, ++g) {
+        for (int j = it.j0; j < it.nt_all; ++j, ++g) {
           const int stage = g % NS;
           const uint32_t phase = (g / NS) & 1;
           const int key0 = j * kChunkKeys;
@@ -233,7 +238,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             ent[p] = -1;
             if (sb < nsb && pos < it.nk_all) {
               const int lb = pos / a.bs;
-              ent[p] = lb >= a.max_blocks ? -2 : (lb < kEntryCache ? ecache[lb] : __ldg(row + lb));
+              ent[p] = lb >= a.max_blocks ? -2
+                                          : (lb - e0 < n_ent ? ecache[lb - e0] : __ldg(row + lb));
             }
           }
           uint32_t nvalid = 0;
@@ -330,17 +336,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int t = 0; t < 2; ++t)
           if (nt_t[t] > 0) issue_s(t, g);
         commit(bar(SM::bKEmpty + g % NS));
-        for (int j = 0; j < it.nt_all && ok; ++j) {
-          const uint32_t gj = g + j;
+        for (int j = it.j0; j < it.nt_all && ok; ++j) {
+          const uint32_t gj = g + (j - it.j0);
           const int stage = gj % NS;
           wait(bar(SM::bVFull + stage), (gj / NS) & 1);
           const uint64_t vd = v_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
 #pragma unroll 1
           for (int t = 0; t < 2; ++t) {
             if (j >= nt_t[t]) continue;
-            const uint32_t tt = gx[t] + j;
+            const uint32_t tt = gx[t] + (j - it.j0);
             wait(bar(SM::bPFull + t), tt & 1);
-            if (j == 0 && kx[t] > 0) wait(bar(SM::bOFree + t), (kx[t] - 1) & 1);
+            if (j == it.j0 && kx[t] > 0) wait(bar(SM::bOFree + t), (kx[t] - 1) & 1);
             tc_fence_after();
             const uint32_t p_t = tmem + t * 128;
             const uint32_t o_t = tmem + 256 + t * D;
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kChunkKeys / 16; ++kk)
                 tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+                          (j > it.j0 || kk > 0) ? 1u : 0u);
               if (j == nt_t[t] - 1) tc_commit(bar(SM::bOFinal + t));
             }
             __syncwarp();
@@ -358,10 +364,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           if (j + 1 < it.nt_all) commit(bar(SM::bKEmpty + (gj + 1) % NS));
           if (j == it.nt_all - 1) commit(bar(SM::bQEmpty));
         }
-        g += it.nt_all;
+        g += it.nt_all - it.j0;
         for (int t = 0; t < 2; ++t) {
           if (nt_t[t] > 0) {
-            gx[t] += nt_t[t];
+            gx[t] += nt_t[t] - it.j0;
             kx[t] += 1;
           }
         }
@@ -387,15 +393,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (item < 0) break;
       const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
       const uint32_t g_item = g;
-      g += it.nt_all;
+      g += it.nt_all - it.j0;
       if (t == 1 && !it.hasB) continue;
       const int nt = it.nt[t];
       const int diag0 = it.ctx + (it.tok[t] - a.cu_seqlens_q[it.s]);  // row 0's last key
       const int limit = diag0 + r;                                     // row r's last key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      for (int j = 0; j < nt; ++j) {
-        const uint32_t tt = gx + j;
+      const int W = a.window;
+      for (int j = it.j0; j < nt; ++j) {
+        const uint32_t tt = gx + (j - it.j0);
         const uint32_t s_col = t * 128;
         if (!mbar_wait(bar(SM::bSFull + t), tt & 1)) { report(a.err, kErrTimeout); ok = false; break; }
         __syncwarp();
@@ -405,10 +412,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + s_col + i * 32, sr + i * 32);
         tc_wait_ld();
         const int key0 = j * kChunkKeys;
-        if (key0 + kChunkKeys - 1 > diag0) {
+        // causal edge (keys past the row's position) and, with a sliding window, its lower
+        // edge (keys at or before position - W)
+        const int lo_r = W > 0 ? limit - W + 1 : 0;
+        if (key0 + kChunkKeys - 1 > diag0 || key0 < lo_r) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (key0 + c > limit) sr[c] = __float_as_uint(-INFINITY);
+            if (key0 + c > limit || key0 + c < lo_r) sr[c] = __float_as_uint(-INFINITY);
         }
         float mx8[8];
 #pragma unroll
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const float mt = mx * sl2;
         float alpha = 1.f;
         bool resc = false;
-        if (j == 0) {
+        if (j == it.j0) {
           m_run = mt;
         } else if (mt > m_run + 8.f) {
           alpha = fast_exp2(m_run - mt);
@@ -432,10 +442,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         float sm8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sm8[i] = 0.f;
+        // A row whose keys so far all lie outside its sliding window has m = -inf: subtract
+        // 0 instead (every p is then 0), so that no -inf - (-inf) appears.
+        const float m_sub = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_run));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_run));
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_sub));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_sub));
           sm8[(c >> 1) & 7] += p0 + p1;
           sr[c >> 1] = pack_bf16x2(p0, p1);
         }
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           // product reads them (both groups may do it; they write the same zeros).
           const int first = it.nk_all - key0;  // 1..128
           if (first < kChunkKeys) {
-            const uint32_t gk = g_item + j;
+            const uint32_t gk = g_item + (j - it.j0);
             const int stage = gk % NS;
             if (!mbar_wait(bar(SM::bVFull + stage), (gk / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
             const uint32_t vst = sbase + SM::kStage0 + stage * SM::kStageBytes + SM::kKVTile;
@@ -507,7 +520,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head[t]] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(bar(SM::bOFree + t));
-      gx += nt;
+      gx += nt - it.j0;
       kx += 1;
     }
   }

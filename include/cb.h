@@ -134,6 +134,12 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
  *                 planner, [1] after it, [2] after the decode kernel (which also merges split
  *                 sequences), and [3] / [4] just before / after the chunk kernel on the stream
  *                 that runs it, so cudaEventElapsedTime gives each kernel's device time.
+ *   window        0: full causal attention.  W > 0: sliding-window attention, for models with
+ *                 sliding-window layer groups (named in "Continuous batching in transformers",
+ *                 paged-cache section, which does not define the mask; this is the common
+ *                 definition): the query at absolute position p sees keys j with
+ *                 p - W < j <= p, i.e. itself and the W - 1 keys before it.  Keys older than
+ *                 the window are not read (neither pass streams them).
  *
  * Concurrency: by default the decode kernel (HBM-bound) runs on `stream` while the chunk kernel
  * (tensor-bound) runs on a second stream that the library creates once per device, forked from
@@ -146,7 +152,9 @@ typedef struct {
   int32_t decode_ctas;
   int32_t flags;
   void* const* phase_events;
-  int64_t reserved[4];
+  int32_t window;        /* > 0: sliding-window attention over the last `window` keys */
+  int32_t reserved32;
+  int64_t reserved[3];
 } cb_options;
 
 #define CB_MAX_DECODE_CTAS 512

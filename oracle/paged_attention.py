@@ -162,11 +162,12 @@ def stable_softmax(x: np.ndarray, axis: int = -1):
     return e / z, np.squeeze(m + np.log(z), axis=axis)
 
 
-def attention_one_sequence(q, K, V, ctx: int, scale: float):
+def attention_one_sequence(q, K, V, ctx: int, scale: float, window: int = 0):
     """Exact causal attention of one sequence's queries over its gathered keys.
 
     q [n, Hq, D] float64 (query i at absolute position ctx + i),
     K, V [kv, Hkv, D] float64 with kv >= ctx + n.
+    window > 0: sliding window, query at position p sees keys j with p - window < j <= p.
     Returns out [n, Hq, D] and lse [n, Hq] (natural log of the softmax normaliser
     of the scaled scores).
     """
@@ -180,7 +181,10 @@ def attention_one_sequence(q, K, V, ctx: int, scale: float):
     if n == 0:
         return out, lse
     # visible[i, j]: key j is at or before query i's absolute position ctx + i.
-    visible = np.arange(kv)[None, :] <= (ctx + np.arange(n))[:, None]
+    pos = (ctx + np.arange(n))[:, None]
+    visible = np.arange(kv)[None, :] <= pos
+    if window > 0:
+        visible &= np.arange(kv)[None, :] > pos - window
     for h in range(Hq):
         g = h // G
         scores = scale * (q[:, h, :] @ K[:, g, :].T)            # [n, kv]
@@ -191,7 +195,7 @@ def attention_one_sequence(q, K, V, ctx: int, scale: float):
 
 
 def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
-                           block_size: int, scale: float):
+                           block_size: int, scale: float, window: int = 0):
     """Attention over a ragged batch whose K/V live in pages.
 
     q: bf16 bits [T, Hq, D]; pages: bf16 bits [P, bs, Hkv, D] (after the append).
@@ -212,14 +216,14 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
         K = gather_kv(k_pages, block_table[s], int(kv[s]), bs)
         V = gather_kv(v_pages, block_table[s], int(kv[s]), bs)
         qs = bf16_bits_to_f64(q[cu[s]:cu[s] + n])
-        o, l = attention_one_sequence(qs, K, V, int(kv[s]) - n, scale)
+        o, l = attention_one_sequence(qs, K, V, int(kv[s]) - n, scale, window)
         out[cu[s]:cu[s] + n] = o
         lse[cu[s]:cu[s] + n] = l
     return out, lse
 
 
 def attention_rows(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size: int,
-                   scale: float, rows):
+                   scale: float, rows, window: int = 0):
     """out/lse for selected (token, head) pairs only: [(t, h), ...] -> (out [n, D], lse [n]).
 
     Used to check a sample of a batch too large to run whole; each row is the
@@ -242,8 +246,9 @@ def attention_rows(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, bloc
         K, V = cache[s]
         g = h // G
         qv = bf16_bits_to_f64(q[t, h])
-        x = scale * (K[: ctx + i + 1, g, :] @ qv)
+        lo = max(0, ctx + i + 1 - window) if window > 0 else 0
+        x = scale * (K[lo: ctx + i + 1, g, :] @ qv)
         p, l = stable_softmax(x)
-        res_o.append(p @ V[: ctx + i + 1, g, :])
+        res_o.append(p @ V[lo: ctx + i + 1, g, :])
         res_l.append(float(l))
     return np.asarray(res_o), np.asarray(res_l)

@@ -238,3 +238,43 @@ def test_configs_full_size(cuda_lib, cfg):
         h_idx = [h for _, h in rows]
         assert_close(gpu[t_idx, h_idx], ref, b.name)
         assert_close(lse.cpu().numpy()[t_idx, h_idx], ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
+
+
+# ----------------------------------------------------------------------------- sliding window
+
+@pytest.mark.parametrize("window", [1, 16, 100, 128, 129, 700])
+@pytest.mark.parametrize("G", [1, 4])
+def test_sliding_window(cuda_lib, window, G):
+    # decodes and chunks whose windows start inside, at and across 16-key decode tiles and
+    # 128-key chunk tiles; G = 1 pairs query tiles, G = 4 pairs heads
+    q_lens = [1, 1, 1, 300, 130, 2, 1]
+    kv_lens = [1, 40, 1500, 300 + 900, 130, 2 + 517, 2000]
+    b = workloads.build_batch(q_lens, kv_lens, 2 * G, 2, 128, 16, seed=600 + window + G,
+                              name=f"window {window} G{G}")
+    db = DeviceBatch(b)
+    db.append()
+    out, lse = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
+                                         db.kv_lens, b.block_size, b.scale, lse=True,
+                                         window=window)
+    assert cb.get_device_error() == cb.CB_OK
+    kp, vp = oracle_append(b)
+    ref, ref_lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
+                                              b.kv_lens, b.block_size, b.scale, window=window)
+    assert_close(out.float().cpu().numpy(), ref, f"window {window}")
+    assert_close(lse.cpu().numpy(), ref_lse, f"window {window} lse", atol=1e-3, rtol=1e-3)
+
+
+def test_sliding_window_d64_split_decode(cuda_lib):
+    b = workloads.build_batch([1, 1, 64], [3000, 70, 64 + 250], 8, 2, 64, 32, seed=611,
+                              name="window D64")
+    db = DeviceBatch(b)
+    db.append()
+    for ctas in (1, 97):
+        out = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
+                                        db.kv_lens, b.block_size, b.scale, window=300,
+                                        decode_ctas=ctas)
+        assert cb.get_device_error() == cb.CB_OK
+        kp, vp = oracle_append(b)
+        ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
+                                            b.kv_lens, b.block_size, b.scale, window=300)
+        assert_close(out.float().cpu().numpy(), ref, f"window D64 ctas {ctas}")

@@ -340,3 +340,47 @@ def test_gather_matches_scalar_slot_rule():
             assert np.array_equal(K[j], _f64(flat[slot]), equal_nan=True)
     with pytest.raises(OracleError):
         opa.gather_kv(b.k_pages, b.block_table[0], 10 ** 4, b.block_size)
+
+
+# ----------------------------------------------------------------------------- sliding window
+
+@pytest.mark.parametrize("window", [1, 3, 16, 40])
+def test_sliding_window_matches_sdpa_with_a_band_mask(window):
+    """Sliding window W: query at position p sees keys (p - W, p].  Against the library
+    attention routine with the equivalent boolean band mask (float64)."""
+    ctx, n, H, D, bs = 30, 17, 2, 8, 4
+    b, kp, vp = _single_sequence(n, ctx + n, H, H, D, bs, seed=21, shuffle=True)
+    cu, kv = b.cu_seqlens_q, b.kv_lens
+    out, lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, cu, kv, bs, b.scale,
+                                          window=window)
+    K = torch.from_numpy(opa.gather_kv(kp, b.block_table[0], ctx + n, bs)).permute(1, 0, 2)
+    V = torch.from_numpy(opa.gather_kv(vp, b.block_table[0], ctx + n, bs)).permute(1, 0, 2)
+    q = torch.from_numpy(_f64(b.q)).permute(1, 0, 2)
+    pos = torch.arange(ctx, ctx + n)[:, None]
+    keys = torch.arange(ctx + n)[None, :]
+    band = (keys <= pos) & (keys > pos - window)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, K, V, attn_mask=band, scale=b.scale)
+    assert np.allclose(out, ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+    rows = [(t, h) for t in range(n) for h in range(H)]
+    ro, rl = opa.attention_rows(b.q, kp, vp, b.block_table, cu, kv, bs, b.scale, rows, window=window)
+    assert np.allclose(ro, out.reshape(-1, D), rtol=0, atol=1e-12)
+    assert np.allclose(rl, lse.reshape(-1), rtol=0, atol=1e-12)
+
+
+def test_sliding_window_closed_forms():
+    ctx, n, H, D, bs = 9, 5, 2, 4, 4
+    b, kp, vp = _single_sequence(n, ctx + n, H, H, D, bs, seed=22, shuffle=False)
+    K = opa.gather_kv(kp, b.block_table[0], ctx + n, bs)
+    V = opa.gather_kv(vp, b.block_table[0], ctx + n, bs)
+    # W = 1: every query sees only its own key, so out = its own value row
+    out, lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                          bs, b.scale, window=1)
+    for i in range(n):
+        assert np.allclose(out[i], V[ctx + i], rtol=0, atol=1e-12)
+        assert np.allclose(lse[i], b.scale * np.sum(_f64(b.q)[i] * K[ctx + i], axis=-1), atol=1e-12)
+    # a window at least as long as the sequence is the full causal pass
+    full, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                         bs, b.scale)
+    wide, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                         bs, b.scale, window=ctx + n)
+    assert np.array_equal(full, wide)
