@@ -82,6 +82,7 @@ __device__ __forceinline__ int pf_heads_per_unit(const AttnArgs& a) {
   return pf_pair_heads(a.G) ? a.Hq / 2 : a.Hq;
 }
 
+template <bool kWin>
 __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
                                                  const int32_t* pf_seq, const int32_t* pf_prefix,
                                                  const int32_t* pf_order, int n_pf) {
@@ -124,11 +125,13 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
   it.nk_all = max(it.nk[0], it.nk[1]);
   it.nt_all = max(it.nt[0], it.nt[1]);
   // tile A's first row is the item's earliest query; keys before its window are not needed
-  it.j0 = window_first_key(it.ctx + qt[0] * kPrefillTileM, a.window) / kChunkKeys;
+  it.j0 = kWin ? window_first_key(it.ctx + qt[0] * kPrefillTileM, a.window) / kChunkKeys : 0;
   return it;
 }
 
-template <int D>
+// kWin: sliding-window attention (a.window > 0).  The full causal pass is compiled without
+// the window's bookkeeping, so it runs exactly the code it ran before windows existed.
+template <int D, bool kWin>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item < 0) break;
-        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+        const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
         if (lane == 0) {
           if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
           mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kQTile);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
         if (item < 0) break;
-        const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+        const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
         const int nt_t[2] = {it.nt[0], it.hasB ? it.nt[1] : 0};
         wait(bar(SM::bQFull), k & 1);
         tc_fence_after();
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
       if (item < 0) break;
-      const PfItem it = pf_decode_item(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+      const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
       const uint32_t g_item = g;
       g += it.nt_all - it.j0;
       if (t == 1 && !it.hasB) continue;
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const int limit = diag0 + r;                                     // row r's last key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
-      const int W = a.window;
+      const int W = kWin ? a.window : 0;
       for (int j = it.j0; j < nt; ++j) {
         const uint32_t tt = gx + (j - it.j0);
         const uint32_t s_col = t * 128;
@@ -414,11 +417,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int key0 = j * kChunkKeys;
         // causal edge (keys past the row's position) and, with a sliding window, its lower
         // edge (keys at or before position - W)
-        const int lo_r = W > 0 ? limit - W + 1 : 0;
-        if (key0 + kChunkKeys - 1 > diag0 || key0 < lo_r) {
+        const int lo_r = kWin ? limit - W + 1 : 0;
+        if (key0 + kChunkKeys - 1 > diag0 || (kWin && key0 < lo_r)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (key0 + c > limit || key0 + c < lo_r) sr[c] = __float_as_uint(-INFINITY);
+            if (key0 + c > limit || (kWin && key0 + c < lo_r)) sr[c] = __float_as_uint(-INFINITY);
         }
         float mx8[8];
 #pragma unroll
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int i = 0; i < 8; ++i) sm8[i] = 0.f;
         // A row whose keys so far all lie outside its sliding window has m = -inf: subtract
         // 0 instead (every p is then 0), so that no -inf - (-inf) appears.
-        const float m_sub = m_run == -INFINITY ? 0.f : m_run;
+        const float m_sub = (kWin && m_run == -INFINITY) ? 0.f : m_run;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_sub));
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kWin>
 static cudaError_t launch_prefill_d(const AttnArgs& a, const CUtensorMap& qmap,
                                     const CUtensorMap& kmap, const CUtensorMap& vmap,
                                     cudaStream_t stream) {
@@ -542,19 +545,23 @@ static cudaError_t launch_prefill_d(const AttnArgs& a, const CUtensorMap& qmap,
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWin>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  prefill_kernel<D><<<a.prefill_ctas, kPrefillThreads, SM::kTotal, stream>>>(a, qmap, kmap, vmap);
+  prefill_kernel<D, kWin><<<a.prefill_ctas, kPrefillThreads, SM::kTotal, stream>>>(a, qmap, kmap, vmap);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream) {
-  if (a.D == 128) return launch_prefill_d<128>(a, qmap, kmap, vmap, stream);
-  return launch_prefill_d<64>(a, qmap, kmap, vmap, stream);
+  if (a.window > 0) {
+    if (a.D == 128) return launch_prefill_d<128, true>(a, qmap, kmap, vmap, stream);
+    return launch_prefill_d<64, true>(a, qmap, kmap, vmap, stream);
+  }
+  if (a.D == 128) return launch_prefill_d<128, false>(a, qmap, kmap, vmap, stream);
+  return launch_prefill_d<64, false>(a, qmap, kmap, vmap, stream);
 }
 
 }  // namespace cb
