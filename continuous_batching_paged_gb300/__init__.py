@@ -92,6 +92,8 @@ def _declare(lib: ctypes.CDLL) -> None:
                                                       ctypes.POINTER(CbDims), _P]
     lib.cb_get_device_error.restype = ctypes.c_int
     lib.cb_get_device_error.argtypes = [_P]
+    lib.cb_selftest_wait_timeout.restype = ctypes.c_int
+    lib.cb_selftest_wait_timeout.argtypes = [ctypes.c_int32, _P, _P]
     lib.cb_copy_blocks.restype = ctypes.c_int
     lib.cb_copy_blocks.argtypes = [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
                                    ctypes.POINTER(CbDims), _P]
@@ -182,6 +184,13 @@ def _check_ids(name, t):
     import torch
     _require(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(),
              f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def selftest_wait_timeout(limit_us: int, waited_ns=None, stream=None) -> None:
+    """Launch one GPU wait that nothing completes; it gives up after limit_us and records
+    CB_ERR_TIMEOUT for get_device_error() (cb_selftest_wait_timeout)."""
+    _check(library().cb_selftest_wait_timeout(int(limit_us), _ptr(waited_ns), _stream(stream)),
+           "cb_selftest_wait_timeout")
 
 
 def copy_blocks(k_pages, v_pages, src, dst, block_size, stream=None) -> None:

@@ -380,6 +380,20 @@ cb_status cb_kv_restore(void* k_pages, void* v_pages, const int32_t* blocks, int
                     cb::kMoveRestore, stream);
 }
 
+cb_status cb_selftest_wait_timeout(int32_t limit_us, unsigned long long* waited_ns, void* stream) {
+  t_last_error.clear();
+  if (limit_us < 1 || limit_us > 100000)
+    return fail(CB_ERR_INVALID_ARG, "limit_us must be in [1, 100000], got %d", limit_us);
+  DeviceState* ds = nullptr;
+  cb_status st = device_state(&ds);
+  if (st != CB_OK) return st;
+  cudaError_t e = cb::launch_wait_selftest(ds->err, (uint64_t)limit_us * 1000ull,
+                                           reinterpret_cast<uint64_t*>(waited_ns),
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return CB_OK;
+}
+
 cb_status cb_get_device_error(void* stream) {
   t_last_error.clear();
   DeviceState* ds = nullptr;

@@ -62,4 +62,23 @@ cudaError_t launch_block_move(const BlockMoveArgs& a, int sm_count, cudaStream_t
   return cudaGetLastError();
 }
 
+// Self-test of the bounded wait every kernel of the library uses: one thread waits on an
+// mbarrier phase that nothing completes; after limit_ns it gives up, records the timeout in
+// the error word and returns, leaving the context usable.
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns, uint64_t* waited_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  const uint64_t t0 = globaltimer_ns();
+  if (!mbar_wait_for(b, 0, limit_ns)) report(err, kErrTimeout);
+  if (waited_ns != nullptr) *waited_ns = globaltimer_ns() - t0;
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, uint64_t* waited_ns,
+                                 cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 1, 0, stream>>>(err, limit_ns, waited_ns);
+  return cudaGetLastError();
+}
+
 }  // namespace cb

@@ -53,6 +53,8 @@ struct BlockMoveArgs {
 
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_block_move(const BlockMoveArgs& a, int sm_count, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, uint64_t* waited_ns,
+                                 cudaStream_t stream);
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);

@@ -234,6 +234,16 @@ cb_status cb_kv_restore(void* k_pages, void* v_pages, const int32_t* blocks, int
  */
 cb_status cb_get_device_error(void* stream);
 
+/*
+ * cb_selftest_wait_timeout -- exercise the failure path every kernel of the library shares,
+ * without a fault: one GPU thread waits on an mbarrier phase that nothing completes; after
+ * limit_us (1 .. 100000) microseconds of %globaltimer it gives up, records CB_ERR_TIMEOUT in
+ * the device error word (read it with cb_get_device_error) and returns, leaving the context
+ * usable.  The kernels' own waits give up the same way after 1 s.  waited_ns: NULL or device
+ * memory for one uint64, the time the wait lasted.  No counterpart on the pages (a test hook).
+ */
+cb_status cb_selftest_wait_timeout(int32_t limit_us, unsigned long long* waited_ns, void* stream);
+
 /* Static English name of a status code (never NULL). */
 const char* cb_status_string(cb_status status);
 

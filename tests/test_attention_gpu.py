@@ -278,3 +278,14 @@ def test_sliding_window_d64_split_decode(cuda_lib):
         ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
                                             b.kv_lens, b.block_size, b.scale, window=300)
         assert_close(out.float().cpu().numpy(), ref, f"window D64 ctas {ctas}")
+
+
+def test_bounded_wait_times_out_without_fault(cuda_lib):
+    # the library's failure path, exercised without a fault: a wait that nothing completes
+    # gives up after its limit, the host reads CB_ERR_TIMEOUT, and the context stays usable
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    cb.selftest_wait_timeout(2000, waited)
+    assert cb.get_device_error() == cb.CB_ERR_TIMEOUT
+    assert 2_000_000 <= int(waited.item()) < 1_000_000_000
+    assert cb.get_device_error() == cb.CB_OK          # read and cleared
+    _run_full(named_config(1))
