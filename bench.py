@@ -64,6 +64,9 @@ def parse_args():
                         "offload / restore kernels; serve: a scheduler-driven serving loop; "
                         "graphs: step latency eager vs CUDA-graph replay")
     p.add_argument("--policy", choices=["fifo", "prefill_first"], default="fifo")
+    p.add_argument("--separate", action="store_true",
+                   help="issue the append and the attention pass as two calls instead of "
+                        "cb_append_attention")
     p.add_argument("--window", type=int, default=0,
                    help="sliding-window attention over the last W keys (0: full causal)")
     return p.parse_args()
@@ -649,11 +652,13 @@ def main():
         e.record()
 
     def step(record):
-        cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
-        cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, out=out,
-                                  workspace=ws, decode_ctas=args.decode_ctas,
-                                  phase_events=ph if record else None, serial=args.serial,
-                                  window=args.window)
+        kw = dict(out=out, workspace=ws, decode_ctas=args.decode_ctas,
+                  phase_events=ph if record else None, serial=args.serial, window=args.window)
+        if args.separate:
+            cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
+            cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, **kw)
+        else:
+            cb.append_attention(q, kn, vn, kp, vp, table, cu, kvl, b.block_size, b.scale, **kw)
 
     # correctness guard before timing: the error word must be clear after one step
     step(False)
@@ -697,8 +702,12 @@ def main():
     value = world * b.num_tokens / (ms / 1000.0)
 
     # Kernel spans (roofline inputs): the same steps again with the library's phase events.
-    spans = {"append": (ev_start, ph[0]), "plan": (ph[0], ph[1]), "decode": (ph[1], ph[2]),
-             "chunk": (ph[3], ph[4])}
+    if args.separate or args.serial:
+        spans = {"append": (ev_start, ph[0]), "plan": (ph[0], ph[1]), "decode": (ph[1], ph[2]),
+                 "chunk": (ph[3], ph[4])}
+    else:  # the planner runs beside the append: one span for both
+        spans = {"append+plan": (ev_start, ph[1]), "decode": (ph[1], ph[2]),
+                 "chunk": (ph[3], ph[4])}
     acc = {n: 0.0 for n in spans}
     n_span = max(1, min(args.steps, 30))
     for _ in range(n_span):
@@ -777,10 +786,13 @@ def main():
             h2d_done[j].record(s_in)
         comp.wait_event(h2d_done[j])
         comp.wait_event(d2h_done[j])               # out buffer j has been read back
-        cb.kv_append(bk, bv, kp, vp, btab, bcu, bkv, b.block_size)
-        cb.ragged_paged_attention(bq, kp, vp, btab, bcu, bkv, b.block_size, b.scale, out=bo,
-                                  workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial,
-                                  window=args.window)
+        kw = dict(out=bo, workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial,
+                  window=args.window)
+        if args.separate:
+            cb.kv_append(bk, bv, kp, vp, btab, bcu, bkv, b.block_size)
+            cb.ragged_paged_attention(bq, kp, vp, btab, bcu, bkv, b.block_size, b.scale, **kw)
+        else:
+            cb.append_attention(bq, bk, bv, kp, vp, btab, bcu, bkv, b.block_size, b.scale, **kw)
         comp_done[j].record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[j])
@@ -838,6 +850,7 @@ def main():
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": world * b.num_tokens / (e2e_serial_ms / 1000.0)},
         "gpu_launches": 4 * args.steps,  # append, plan, decode (with merge), chunk per step
+        "append_attention": "two calls" if args.separate else "cb_append_attention",
         "concurrent_decode_chunk": not args.serial,
         "roofline": roof,
         "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,

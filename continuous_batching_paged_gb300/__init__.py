@@ -21,6 +21,7 @@ __all__ = [
     "CB_ERR_TIMEOUT", "CB_ERR_CUDA", "CbDims", "CbOptions", "library", "library_path",
     "kv_append", "ragged_paged_attention", "workspace_size", "get_device_error",
     "check_device_error", "status_string", "copy_blocks", "kv_offload", "kv_restore",
+    "append_attention", "selftest_wait_timeout",
 ]
 
 CB_OK = 0
@@ -86,6 +87,11 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.cb_ragged_paged_attention.argtypes = attn + [_P]
     lib.cb_ragged_paged_attention_ex.restype = ctypes.c_int
     lib.cb_ragged_paged_attention_ex.argtypes = attn + [ctypes.POINTER(CbOptions), _P]
+    lib.cb_append_attention.restype = ctypes.c_int
+    lib.cb_append_attention.argtypes = [_P, _P, _P, _P] + [_P, _P, _P, _P, ctypes.c_int32,
+                                                          ctypes.c_float, _P, _P, _P,
+                                                          ctypes.c_size_t, ctypes.POINTER(CbDims),
+                                                          ctypes.POINTER(CbOptions), _P]
     lib.cb_ragged_paged_attention_noalloc.restype = ctypes.c_int
     lib.cb_ragged_paged_attention_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_int32,
                                                       ctypes.c_float, _P, _P,
@@ -258,7 +264,7 @@ def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max
 def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size,
                            scale, out=None, lse=None, workspace=None, decode_ctas: int = 0,
                            phase_events=None, serial: bool = False, window: int = 0,
-                           stream=None):
+                           stream=None, k_new=None, v_new=None):
     """One attention pass over the ragged batch (cb_ragged_paged_attention_ex).
 
     q [T, Hq, D] bf16; pages [P, bs, Hkv, D] bf16 (after the append); returns out [T, Hq, D]
@@ -301,12 +307,33 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
         handles = (ctypes.c_void_p * NUM_PHASE_EVENTS)(*[int(e.cuda_event) for e in phase_events])
         _require(all(handles), "phase events must have been recorded once (created) before use")
         opts.phase_events = ctypes.cast(handles, ctypes.POINTER(ctypes.c_void_p))
-    st = library().cb_ragged_paged_attention_ex(
-        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(cu_seqlens_q),
-        _ptr(kv_lens), int(block_size), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel(), ctypes.byref(dims), ctypes.byref(opts), _stream(stream))
-    _check(st, "cb_ragged_paged_attention")
+    if k_new is None:
+        st = library().cb_ragged_paged_attention_ex(
+            _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(cu_seqlens_q),
+            _ptr(kv_lens), int(block_size), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel(), ctypes.byref(dims), ctypes.byref(opts), _stream(stream))
+        _check(st, "cb_ragged_paged_attention")
+    else:
+        _check_bf16("k_new", k_new, 3)
+        _check_bf16("v_new", v_new, 3)
+        _require(tuple(k_new.shape) == (T, Hkv, D) and k_new.shape == v_new.shape,
+                 "k_new / v_new must be [T, Hkv, D]")
+        st = library().cb_append_attention(
+            _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages), _ptr(q), _ptr(block_table),
+            _ptr(cu_seqlens_q), _ptr(kv_lens), int(block_size), float(scale), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel(), ctypes.byref(dims),
+            ctypes.byref(opts), _stream(stream))
+        _check(st, "cb_append_attention")
     return (out, lse) if want_lse else out
+
+
+def append_attention(q, k_new, v_new, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
+                     block_size, scale, **kwargs):
+    """kv_append then ragged_paged_attention in one call (cb_append_attention): same results,
+    with the attention planner overlapping the append.  Keyword arguments as for
+    ragged_paged_attention."""
+    return ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
+                                  block_size, scale, k_new=k_new, v_new=v_new, **kwargs)
 
 
 def get_device_error(stream=None) -> int:

@@ -39,6 +39,8 @@ struct DeviceState {
   cudaStream_t aux = nullptr;      // second stream for the chunk kernel (created once)
   cudaEvent_t ev_fork = nullptr;   // timing-free fork / join events (created once)
   cudaEvent_t ev_join = nullptr;
+  cudaEvent_t ev_plan = nullptr;   // fused append + attention: planner done, append done
+  cudaEvent_t ev_append = nullptr;
   std::mutex launch_mu;            // one fork/join sequence at a time per device
 };
 
@@ -70,6 +72,8 @@ cb_status device_state(DeviceState** out) {
     e = cudaStreamCreateWithFlags(&st.aux, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_plan, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_append, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "creating the library's stream and events");
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
@@ -204,13 +208,15 @@ cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void
   return CB_OK;
 }
 
-cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const void* v_pages,
-                                       const int32_t* block_table, const int32_t* cu_seqlens_q,
-                                       const int32_t* kv_lens, int32_t block_size, float scale,
-                                       void* out, float* lse, void* workspace,
-                                       size_t workspace_bytes, const cb_dims* dims,
-                                       const cb_options* options, void* stream) {
-  t_last_error.clear();
+// The attention pass; with `app` non-NULL the KV-append of the same step is launched in the
+// same sequence, on the caller's stream while the planner (which reads only the metadata) runs
+// on the second stream, and both attention kernels wait for both.
+static cb_status attention(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* block_table, const int32_t* cu_seqlens_q,
+                           const int32_t* kv_lens, int32_t block_size, float scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes,
+                           const cb_dims* dims, const cb_options* options,
+                           const cb::AppendArgs* app, void* stream) {
   cb_status st = check_dims(dims, block_size);
   if (st != CB_OK) return st;
   if (dims->num_tokens == 0) return CB_OK;
@@ -285,30 +291,107 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
     return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), on) : cudaSuccess;
   };
   std::lock_guard<std::mutex> lk(ds->launch_mu);
-  cudaError_t e = mark(0, s);
-  if (e == cudaSuccess && (e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
-  if (e == cudaSuccess) e = mark(1, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-  cudaStream_t cs = serial ? s : ds->aux;
-  if (!serial) {
-    // fork: the chunk kernel's stream waits for the planner
+  cudaError_t e = cudaSuccess;
+  cudaStream_t cs = serial ? s : ds->aux;  // chunk kernel's stream
+  cudaStream_t dstr = s;                   // decode kernel's stream
+  if (app != nullptr && !serial) {
+    // Fork before the append: the planner runs on the second stream beside the append on the
+    // caller's.  The decode kernel then follows the planner on the second stream and the chunk
+    // kernel the append on the caller's, each after waiting for the other's predecessor: the
+    // stream that waits on the append's completion is the one whose next launch reaches the
+    // SMs first, and the decode kernel must place its CTAs first.
+    cs = s;
+    dstr = ds->aux;
+    cb::AppendArgs ap = *app;
+    ap.err = ds->err;
     if ((e = cudaEventRecord(ds->ev_fork, s)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(ds->aux, ds->ev_fork, 0)) != cudaSuccess)
-      return cuda_fail(e, "fork to the chunk stream");
+      return cuda_fail(e, "fork to the second stream");
+    if ((e = mark(0, ds->aux)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+    if ((e = cb::launch_plan(a, ds->aux)) != cudaSuccess) return cuda_fail(e, "plan launch");
+    if ((e = cudaEventRecord(ds->ev_plan, ds->aux)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventRecord(plan)");
+    if ((e = cb::launch_kv_append(ap, s)) != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    if ((e = cudaStreamWaitEvent(s, ds->ev_plan, 0)) != cudaSuccess ||
+        (e = cudaEventRecord(ds->ev_append, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ds->aux, ds->ev_append, 0)) != cudaSuccess)
+      return cuda_fail(e, "append / planner join");
+    if ((e = mark(1, ds->aux)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  } else {
+    if (app != nullptr) {
+      cb::AppendArgs ap = *app;
+      ap.err = ds->err;
+      if ((e = cb::launch_kv_append(ap, s)) != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    }
+    e = mark(0, s);
+    if (e == cudaSuccess && (e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
+    if (e == cudaSuccess) e = mark(1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+    if (!serial) {
+      // fork: the chunk kernel's stream waits for the planner
+      if ((e = cudaEventRecord(ds->ev_fork, s)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(ds->aux, ds->ev_fork, 0)) != cudaSuccess)
+        return cuda_fail(e, "fork to the chunk stream");
+    }
   }
-  if ((e = cb::launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
-  if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  if ((e = cb::launch_decode(a, kmap, vmap, dstr)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if ((e = mark(2, dstr)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
   if ((e = mark(3, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
   if ((e = cb::launch_prefill(a, qmap, kmap_c, vmap_c, cs)) != cudaSuccess)
     return cuda_fail(e, "prefill launch");
   if ((e = mark(4, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
   if (!serial) {
-    // join: work queued on the caller's stream after this call waits for the chunk kernel
+    // join: work queued on the caller's stream after this call waits for the kernel on the
+    // second stream
     if ((e = cudaEventRecord(ds->ev_join, ds->aux)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(s, ds->ev_join, 0)) != cudaSuccess)
       return cuda_fail(e, "join from the chunk stream");
   }
   return CB_OK;
+}
+
+cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                       const int32_t* kv_lens, int32_t block_size, float scale,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, const cb_dims* dims,
+                                       const cb_options* options, void* stream) {
+  t_last_error.clear();
+  return attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size, scale,
+                   out, lse, workspace, workspace_bytes, dims, options, nullptr, stream);
+}
+
+cb_status cb_append_attention(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                              const void* q, const int32_t* block_table,
+                              const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                              int32_t block_size, float scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, const cb_dims* dims,
+                              const cb_options* options, void* stream) {
+  t_last_error.clear();
+  cb_status st = check_dims(dims, block_size);
+  if (st != CB_OK) return st;
+  if (dims->num_tokens == 0 || dims->num_seqs == 0) return CB_OK;
+  if (!k_new || !v_new) return fail(CB_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k_new) || !aligned16(v_new))
+    return fail(CB_ERR_INVALID_ARG, "K/V tensors must be 16-byte aligned");
+  cb::AppendArgs ap;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_pages = k_pages;
+  ap.v_pages = v_pages;
+  ap.block_table = block_table;
+  ap.cu_seqlens_q = cu_seqlens_q;
+  ap.kv_lens = kv_lens;
+  ap.S = dims->num_seqs;
+  ap.T = dims->num_tokens;
+  ap.Hkv = dims->num_kv_heads;
+  ap.D = dims->head_dim;
+  ap.bs = block_size;
+  ap.max_blocks = dims->max_blocks_per_seq;
+  ap.P = dims->num_pages;
+  ap.err = nullptr;  // set to the device's error word at launch
+  return attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size, scale,
+                   out, lse, workspace, workspace_bytes, dims, options, &ap, stream);
 }
 
 cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const void* v_pages,

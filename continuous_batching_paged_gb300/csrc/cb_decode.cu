@@ -535,6 +535,7 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, cudaStream_t stream) {
   using SM = DecodeSmem<D>;
   static int configured_device = -1;
+  static int top_priority = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
@@ -543,16 +544,28 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SM::kTotal);
+    int least = 0, greatest = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
     if (e != cudaSuccess) return e;
+    top_priority = greatest;
     configured_device = dev;
   }
   const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
-  dim3 grid(a.decode_ctas, (a.Hkv + kMaxDecodeHeadsPerCta - 1) / kMaxDecodeHeadsPerCta);
-  if (a.G <= 8)
-    decode_kernel<D, 1><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
-  else
-    decode_kernel<D, 2><<<grid, 32 * (HB + 1), SM::kTotal, stream>>>(a, kmap, vmap);
-  return cudaGetLastError();
+  // The decode kernel runs at the highest launch priority: when it and the chunk kernel become
+  // ready together, the block scheduler places the decode CTAs first and the chunk kernel's
+  // persistent CTAs take the SMs the planner left free.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributePriority;
+  attr[0].val.priority = top_priority;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.decode_ctas, (a.Hkv + kMaxDecodeHeadsPerCta - 1) / kMaxDecodeHeadsPerCta);
+  cfg.blockDim = dim3(32 * (HB + 1));
+  cfg.dynamicSmemBytes = SM::kTotal;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.G <= 8) return cudaLaunchKernelEx(&cfg, decode_kernel<D, 1>, a, kmap, vmap);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, 2>, a, kmap, vmap);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -17,7 +17,7 @@ from __future__ import annotations
 
 from collections import OrderedDict
 
-from . import kv_append, ragged_paged_attention, workspace_size
+from . import append_attention, workspace_size
 
 
 def _round_up(x: int, m: int) -> int:
@@ -42,9 +42,8 @@ class _Bucket:
                               dtype=torch.uint8, device=dev)
 
         def body():
-            kv_append(self.k, self.v, o.k_pages, o.v_pages, self.table, self.cu, self.kv, o.bs)
-            ragged_paged_attention(self.q, o.k_pages, o.v_pages, self.table, self.cu, self.kv,
-                                   o.bs, o.scale, out=self.out, workspace=self.ws)
+            append_attention(self.q, self.k, self.v, o.k_pages, o.v_pages, self.table, self.cu,
+                             self.kv, o.bs, o.scale, out=self.out, workspace=self.ws)
 
         # One eager pass on a side stream (all sequences empty: nothing is read or written)
         # initialises the library on this device before the capture, then the capture.

@@ -167,6 +167,24 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
                                        const cb_options* options, void* stream);
 
 /*
+ * cb_append_attention -- cb_kv_append followed by cb_ragged_paged_attention_ex in one call, with
+ * the same arguments and the same results (bit for bit).  The attention pass's planner reads
+ * only the metadata, so it runs on the library's second stream while the append runs on
+ * `stream`; the decode and chunk kernels then wait for both (the decode kernel on the second
+ * stream, the chunk kernel on `stream`).  This overlaps the two short launch-bound kernels
+ * that begin every step.  Phase events: [0] / [1] on the second stream before the planner and
+ * before the decode kernel, [2] after it; [3] / [4] around the chunk kernel on `stream`.  k_new / v_new as in cb_kv_append; every other
+ * argument as in cb_ragged_paged_attention_ex (with CB_OPT_SERIAL the four kernels run one
+ * after the other on `stream`).
+ */
+cb_status cb_append_attention(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                              const void* q, const int32_t* block_table,
+                              const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                              int32_t block_size, float scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, const cb_dims* dims,
+                              const cb_options* options, void* stream);
+
+/*
  * cb_ragged_paged_attention_noalloc -- cb_ragged_paged_attention without a workspace argument.
  * (An addition of this library with no counterpart in the pages that describe the method.)
  *

@@ -289,3 +289,21 @@ def test_bounded_wait_times_out_without_fault(cuda_lib):
     assert 2_000_000 <= int(waited.item()) < 1_000_000_000
     assert cb.get_device_error() == cb.CB_OK          # read and cleared
     _run_full(named_config(1))
+
+
+@pytest.mark.parametrize("serial", [False, True])
+@pytest.mark.parametrize("cfg", [1, 3, 4])
+def test_fused_append_attention_equals_separate_calls(cuda_lib, cfg, serial):
+    # cb_append_attention (planner overlapping the append) gives the pools and outputs of the
+    # two separate calls, bit for bit
+    b = named_config(cfg)
+    a, f = DeviceBatch(b), DeviceBatch(b)
+    a.append()
+    out_a = cb.ragged_paged_attention(a.q, a.k_pages, a.v_pages, a.block_table, a.cu,
+                                      a.kv_lens, b.block_size, b.scale, serial=serial)
+    out_f = cb.append_attention(f.q, f.k_new, f.v_new, f.k_pages, f.v_pages, f.block_table,
+                                f.cu, f.kv_lens, b.block_size, b.scale, serial=serial)
+    assert cb.get_device_error() == cb.CB_OK
+    assert torch.equal(out_a.view(torch.int16), out_f.view(torch.int16))
+    assert torch.equal(a.k_pages.view(torch.int16), f.k_pages.view(torch.int16))
+    assert torch.equal(a.v_pages.view(torch.int16), f.v_pages.view(torch.int16))
