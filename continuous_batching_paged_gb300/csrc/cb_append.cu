@@ -154,40 +154,49 @@ __device__ __forceinline__ void block_scan4(int v[4], int ex[4], int tot[4], int
 
 // Decode CTA count for a batch whose chunk pass runs beside the decode pass.  Model, fitted to
 // GB300 measurements of these kernels: decode on N SMs streams its bytes at
-// BW(N) = ((0.105 N)^-3 + 6.45^-3)^(-1/3) TB/s (linear in N until HBM saturates); the chunk pass
-// runs at ~6.6 TFLOP/s per SM on the other SMs meanwhile and on every SM afterwards.  The
-// choice is the largest N within 1% of the modelled minimum step time, so that the decode
-// pass keeps its bandwidth where the curve is flat.  Without chunk work all CTAs decode.
-// Called by one full warp; candidates N = 8, 16, ... are spread over the lanes, in fp32 (the
-// fp64 rate of this part is far too low for even this much arithmetic on one thread).
-__device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int max_ctas, long long tiles) {
+// BW(N) = ((0.11 N)^-3 + 6.8^-3)^(-1/3) TB/s (linear in N until HBM saturates), taking td; the
+// chunk pass runs at ~6.4 TFLOP/s per SM on the other M SMs meanwhile and on every SM
+// afterwards.  Chunk CTAs claim whole items (one query tile of one or two heads against its
+// whole key range), so the chunk pass ends on item boundaries: if its work W fits in M SMs
+// before td it ends near W/M (plus a short longest-first tail); if not, the items still
+// unclaimed when decode ends each take a full item time on the newly free SMs, so the step is
+// td + (W - M td)/SMs + about half an item.  The choice is the largest N within 1% of the
+// modelled minimum, so that the decode pass keeps its bandwidth where the curve is flat.
+// Without chunk work all CTAs decode.  Called by one full warp; candidates
+// N = 4, 8, ... are spread over the lanes, in fp32 (the fp64 rate of this part is far too low
+// for even this much arithmetic on one thread).
+__device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int chunk_items,
+                                  int max_ctas, long long tiles) {
   const int lane = threadIdx.x & 31;
   if (tiles <= 0) return 1;
   const int cap = (int)(tiles < max_ctas ? tiles : max_ctas);
-  if (chunk_flops <= 0.f) return cap;
-  const float w_us = chunk_flops * (1.f / 6.6e6f);  // chunk work in SM-microseconds
+  if (chunk_flops <= 0.f || chunk_items <= 0) return cap;
+  const float w_us = chunk_flops * (1.f / 6.4e6f);  // chunk work in SM-microseconds
+  const float item_us = w_us / (float)chunk_items;
   const float b_mb = dec_bytes * 1e-6f;             // decode bytes / 1e6: MB / (TB/s) = us
-  const int n_cand = (cap + 7) / 8;
-  float t[2];
-  int n[2];
+  const int n_cand = (cap + 3) / 4;
+  float t[4];
+  int n[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 4; ++k) {
     const int i = lane + 32 * k;
-    n[k] = 8 * (i + 1) < cap ? 8 * (i + 1) : cap;
+    n[k] = 4 * (i + 1) < cap ? 4 * (i + 1) : cap;
     t[k] = 3.4e38f;
     if (i < n_cand) {
-      const float lin = 0.105f * n[k], sat = 6.45f;
+      const float lin = 0.11f * n[k], sat = 6.8f;
       const float bw = rcbrtf(1.f / (lin * lin * lin) + 1.f / (sat * sat * sat));
       const float td = b_mb / bw;
-      const float left = w_us - (float)(max_ctas - n[k]) * td;
-      t[k] = td + (left > 0.f ? left / max_ctas : 0.f);
+      const int m = max_ctas - n[k];
+      const float rest = w_us - (float)m * td;  // chunk work not done when decode ends
+      t[k] = rest <= 0.f ? fmaxf(td, w_us / (float)m + 0.15f * item_us)
+                         : td + rest / (float)max_ctas + 0.5f * item_us;
     }
   }
-  float t_min = fminf(t[0], t[1]);
+  float t_min = fminf(fminf(t[0], t[1]), fminf(t[2], t[3]));
   for (int o = 16; o > 0; o >>= 1) t_min = fminf(t_min, __shfl_xor_sync(0xffffffffu, t_min, o));
   int best = 1;
 #pragma unroll
-  for (int k = 0; k < 2; ++k)
+  for (int k = 0; k < 4; ++k)
     if (t[k] <= 1.01f * t_min) best = best > n[k] ? best : n[k];
   for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
   return best;
@@ -356,7 +365,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
     int n = (int)(ntiles < a.decode_ctas ? (ntiles > 0 ? ntiles : 1) : a.decode_ctas);
     if (a.decode_auto)
       n = choose_decode_ctas(keys * (float)(a.Hkv * a.D * 4), pairs * (float)(4 * a.D * a.Hq),
-                             a.decode_ctas, ntiles);
+                             n_units * (pf_pair_heads(a.G) ? a.Hq / 2 : a.Hq), a.decode_ctas,
+                             ntiles);
     if (tid == 0) {
       s_N = n;
       hdr->decode_ctas = n;

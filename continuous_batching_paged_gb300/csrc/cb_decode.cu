@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
 
   const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x, hg = blockIdx.y;
+  const int hg = blockIdx.y;
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
   const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
@@ -420,7 +420,23 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
 
   const long long ntiles = hdr->dec_tiles;
   const int N = hdr->decode_ctas;  // planner's CTA count: <= gridDim.x, every range non-empty
-  if (c >= N) return;
+  // With N below the grid size the working CTAs are spread evenly over the grid, in pairs of
+  // consecutive CTAs where N and the grid are even: CTA b (or pair b/2) works when it is the
+  // first with its value of floor(b N / grid), and takes that value's range.  The block
+  // scheduler puts consecutive CTAs on the two SMs of a TPC and deals TPCs out across the GPCs.
+  // Measured beside a chunk pass: with the first N CTAs working the decode pass ran ~6% slower;
+  // with single CTAs spread, decode and chunk CTAs shared TPCs and the chunk pass ran ~5%
+  // slower; spread pairs ran both at the speed of a launch of exactly N CTAs.
+  const int grid = (int)gridDim.x, bx = (int)blockIdx.x;
+  int c = bx;
+  if (N < grid) {
+    const bool pairs = ((N | grid) & 1) == 0;
+    const int units = pairs ? grid / 2 : grid, wanted = pairs ? N / 2 : N;
+    const int u = pairs ? bx >> 1 : bx;
+    const int cu = (int)((long long)u * wanted / units);
+    if (u > 0 && (long long)(u - 1) * wanted / units == cu) return;
+    c = pairs ? 2 * cu + (bx & 1) : cu;
+  }
   const long long t0 = ntiles * c / N, t1 = ntiles * (c + 1) / N;
   if (t0 >= t1) return;
 
@@ -441,6 +457,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
     }
     const int KB = a.KB;
     const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
+    const uint64_t stream_policy = l2_policy_evict_first();  // each K/V row is read once
     const int tiles_per_batch = 32 / nsb;
     int d = cta_first[c];
     long long t = t0;
@@ -513,10 +530,10 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             const uint32_t off = (uint32_t)(lane * HB * KB * 128);  // run sb: [HB heads][KB keys]
 #pragma unroll
             for (int half = 0; half < SM::kHalves; ++half) {
-              tma_load_3d(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
-                          half * 64, token, hg * kMaxDecodeHeadsPerCta);
-              tma_load_3d(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
-                          half * 64, token, hg * kMaxDecodeHeadsPerCta);
+              tma_load_3d_hint(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
+                               half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
+              tma_load_3d_hint(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
+                               half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
             }
           }
         }

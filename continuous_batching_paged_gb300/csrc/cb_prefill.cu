@@ -423,15 +423,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (key0 + c > limit || (kWin && key0 + c < lo_r)) sr[c] = __float_as_uint(-INFINITY);
         }
+        // row max: 8 independent chains of three-input max over the 128 columns
         float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sr[i]);
+        for (int i = 0; i < 8; ++i)
+          mx8[i] = fmax3(__uint_as_float(sr[i]), __uint_as_float(sr[8 + i]), __uint_as_float(sr[16 + i]));
 #pragma unroll
-        for (int c = 8; c < 128; c += 8)
+        for (int c = 24; c < 120; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], __uint_as_float(sr[c + i]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int i = 0; i < 8; ++i)
+            mx8[i] = fmax3(mx8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], __uint_as_float(sr[120 + i]));
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                               fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float mt = mx * sl2;
         float alpha = 1.f;
         bool resc = false;
@@ -442,19 +447,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           m_run = mt;
           resc = true;
         }
-        float sm8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sm8[i] = 0.f;
         // A row whose keys so far all lie outside its sliding window has m = -inf: subtract
         // 0 instead (every p is then 0), so that no -inf - (-inf) appears.
         const float m_sub = (kWin && m_run == -INFINITY) ? 0.f : m_run;
+        // exponent arguments and row sums two columns per instruction (paired fp32)
+        const uint64_t scale2 = f2_pack(sl2, sl2), neg_m2 = f2_pack(-m_sub, -m_sub);
+        uint64_t sum2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_sub));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_sub));
-          sm8[(c >> 1) & 7] += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, neg_m2),
+                    x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          sum2[(c >> 1) & 3] = f2_add(sum2[(c >> 1) & 3], f2_pack(p0, p1));
           sr[c >> 1] = pack_bf16x2(p0, p1);
         }
+        float sm8[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f2_unpack(sum2[i], sm8[2 * i], sm8[2 * i + 1]);
         const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
         l_run = l_run * alpha + sum;
         if (j == it.nt_all - 1) {
