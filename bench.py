@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the ragged paged-attention hot path on GB300.
 
-One step = one pass of the whole path over one synthetic batch: the paged KV-append
-(cb_kv_append) followed by the ragged paged-attention pass (cb_ragged_paged_attention: planner,
-split-KV decode kernel, LSE merge, tcgen05 chunk kernel).  Default workload: the mixed ragged
+One step = one pass of the whole path over one synthetic batch: the paged KV-append and the
+ragged paged-attention pass (cb_append_attention: append + planner in one launch, then the
+attention kernel, whose CTAs run the split-KV decode pass with its LSE merge and the tcgen05
+chunk pass).  Default workload: the mixed ragged
 batch at max_batch_tokens = 2048 (120 decode tokens at prior context U[256, 8192] plus one
 1928-token chunk at prior context 3000; 32 query / 8 KV heads, head_dim 128, block size 32), the
 one batch of the named set in which every step of the path runs.
@@ -12,8 +13,9 @@ Prints ONE JSON line.  `value` is query tokens per second of the whole job, from
 (CUDA events on the launching stream) with inputs resident in HBM; L2 is flushed (a 512 MiB
 write, then a 512 MiB read) before every timed step.  `e2e` is the same metric through the Python API with the step's
 inputs copied from pinned host memory and the output copied back inside the timed region.
-`roofline` is the dominant kernel's algorithmic bytes (or FLOPs) per launch over its average
-device time, measured by events the library records around each kernel.  `cpu_baseline` is the
+`roofline` is the attention kernel's algorithmic bytes (or FLOPs, by the bound of the pass with
+the larger ideal time) per launch over its average device time, measured by events the library
+records around the launch.  `cpu_baseline` is the
 float64 oracle timed on a bounded sample of the same workload on this host's cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixed|decode|prefill|longtail]
@@ -58,7 +60,7 @@ def parse_args():
     p.add_argument("--decode-ctas", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--serial", action="store_true",
-                   help="run the chunk kernel after the decode kernel instead of concurrently")
+                   help="run the decode pass and the chunk pass as two launches, one after the other")
     p.add_argument("--mode", choices=["path", "blocks", "serve", "graphs"], default="path",
                    help="path: the attention hot path (default); blocks: KV block copy / "
                         "offload / restore kernels; serve: a scheduler-driven serving loop; "
@@ -528,7 +530,7 @@ def run_serve(args, local: int):
                    "new_tokens": "U[64, 512]", "max_batch_tokens": budget,
                    "max_requests_per_batch": cap, "pool_blocks": P, "block_size": bs,
                    "q_heads": Hq, "kv_heads": Hkv, "head_dim": D},
-        "gpu_launches": "5 per step (append, plan, decode, chunk; block copy when needed)",
+        "gpu_launches": "3 per step (append, plan, attention; block copy when needed)",
     }
     print(json.dumps(line), flush=True)
 
@@ -702,13 +704,21 @@ def main():
     value = world * b.num_tokens / (ms / 1000.0)
 
     # Kernel spans (roofline inputs): the same steps again with the library's phase events.
-    if args.separate or args.serial:
+    # In the default (one attention launch) mode the decode and chunk passes share a launch:
+    # the events time that launch, and the passes' own spans inside it come from the device
+    # time stamps the kernel leaves in the workspace (cb_pass_timestamps).
+    if args.serial and args.separate:
         spans = {"append": (ev_start, ph[0]), "plan": (ph[0], ph[1]), "decode": (ph[1], ph[2]),
                  "chunk": (ph[3], ph[4])}
-    else:  # the planner runs beside the append: one span for both
+    elif args.serial:
         spans = {"append+plan": (ev_start, ph[1]), "decode": (ph[1], ph[2]),
                  "chunk": (ph[3], ph[4])}
+    elif args.separate:
+        spans = {"append": (ev_start, ph[0]), "plan": (ph[0], ph[1]), "attention": (ph[1], ph[2])}
+    else:
+        spans = {"append+plan": (ev_start, ph[1]), "attention": (ph[1], ph[2])}
     acc = {n: 0.0 for n in spans}
+    role = {"decode": 0.0, "chunk": 0.0}
     n_span = max(1, min(args.steps, 30))
     for _ in range(n_span):
         flush_l2()
@@ -718,8 +728,12 @@ def main():
         ev_end.synchronize()
         for n, (e0_, e1_) in spans.items():
             acc[n] += e0_.elapsed_time(e1_)
+        ts = cb.pass_timestamps(ws)
+        role["decode"] += (ts[1] - ts[0]) * 1e-6
+        role["chunk"] += (ts[3] - ts[2]) * 1e-6
     cb.check_device_error()
     per_kernel = {n: dist_max(acc[n] / n_span, world, dev) for n in spans}
+    role_ms = {n: dist_max(v / n_span, world, dev) for n, v in role.items()}
 
     # e2e: the step through the public API with inputs from pinned host memory, output back.
     h_q = torch.from_numpy(b.q.view(np.int16)).pin_memory()
@@ -813,25 +827,36 @@ def main():
     pk, pk_kind = peaks()
     dec_bytes, dec_logical = decode_kv_bytes(b, args.window)
     flops = chunk_flops(b, args.window)
-    dec_ms, chunk_ms = per_kernel["decode"], per_kernel["chunk"]
+    # Pass spans: with both passes in one launch, from the kernel's device time stamps; in
+    # serial mode (two launches), from the events around each launch.
+    dec_ms = per_kernel["decode"] if args.serial else role_ms["decode"]
+    chunk_ms = per_kernel["chunk"] if args.serial else role_ms["chunk"]
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 and dec_bytes else None
     chunk_tf = flops / (chunk_ms * 1e-3) / 1e12 if chunk_ms > 0 and flops else None
-    # The dominant kernel is the one with the larger roofline time (work / peak): the chunk
-    # kernel's span runs beside the decode kernel and includes its wait for free SMs.
+    # The roofline is taken on the attention kernel (one launch runs both passes; its span from
+    # the events around it), against the bound of the pass with the larger ideal time (work /
+    # peak).  In serial mode each pass is its own launch and is measured alone.
     dec_ideal = dec_bytes / (pk["hbm_gbs"] * 1e9) if dec_bytes else 0.0
     chunk_ideal = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
-    if dec_gbs is not None and (chunk_tf is None or dec_ideal >= chunk_ideal):
-        roof = {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"],
-                "traffic": recorded_traffic("decode_kernel", args.workload),
-                "algorithmic_bytes_per_launch": dec_bytes,
-                "peak_kind": pk_kind, "frac_of_nominal_8000": dec_gbs / NOMINAL_HBM_GBS}
+    hbm_bound = dec_ideal >= chunk_ideal and dec_bytes > 0
+    if args.serial:
+        attn_ms = dec_ms if hbm_bound else chunk_ms
+    else:
+        attn_ms = per_kernel["attention"]
+    traffic = recorded_traffic("attention_kernel", args.workload)
+    if hbm_bound:
+        ach = dec_bytes / (attn_ms * 1e-3) / 1e9
+        roof = {"kernel": "attention_kernel", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": attn_ms,
+                "peak_kind": pk_kind, "frac_of_nominal_8000": ach / NOMINAL_HBM_GBS}
     else:
         tpk = pk["bf16_tflops"]
-        roof = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": chunk_tf, "peak": tpk,
-                "unit": "TFLOP/s", "frac": chunk_tf / tpk,
-                "traffic": recorded_traffic("prefill_kernel", args.workload),
-                "algorithmic_flops_per_launch": flops, "peak_kind": pk_kind + " burst bf16"}
+        ach = flops / (attn_ms * 1e-3) / 1e12
+        roof = {"kernel": "attention_kernel", "bound": "tensor", "achieved": ach, "peak": tpk,
+                "unit": "TFLOP/s", "frac": ach / tpk, "traffic": traffic,
+                "algorithmic_flops_per_launch": flops, "launch_ms": attn_ms,
+                "peak_kind": pk_kind + " burst bf16"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -849,16 +874,21 @@ def main():
                        "steps' kernels (double buffers, copy streams)",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": world * b.num_tokens / (e2e_serial_ms / 1000.0)},
-        "gpu_launches": 4 * args.steps,  # append, plan, decode (with merge), chunk per step
+        # per step: append + plan (one launch) and attention (decode, merge, chunk in one
+        # launch); --separate: append, plan, attention; --serial: one more (the passes apart)
+        "gpu_launches": (2 + int(args.separate) + int(args.serial)) * args.steps,
         "append_attention": "two calls" if args.separate else "cb_append_attention",
         "concurrent_decode_chunk": not args.serial,
         "roofline": roof,
         "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
-                   "gbs": dec_gbs, "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,
+                   "span_ms": dec_ms, "gbs": dec_gbs,
+                   "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,
                    "frac_of_nominal_8000": (dec_gbs / NOMINAL_HBM_GBS) if dec_gbs else None},
-        "chunk": {"flops": flops, "tflops": chunk_tf,
+        "chunk": {"flops": flops, "span_ms": chunk_ms, "tflops": chunk_tf,
                   "span_note": None if args.serial else
-                  "span runs beside the decode kernel and includes its wait for free SMs",
+                  "decode and chunk spans: first start to last end of each pass's CTAs with work "
+                  "(device %globaltimer stamps, cb_pass_timestamps); the chunk pass runs on the "
+                  "SMs the decode pass leaves free",
                   "frac_of_burst": (chunk_tf / pk["bf16_tflops"]) if chunk_tf else None,
                   "frac_of_sustained": (chunk_tf / pk["bf16_tflops_sustained"]) if chunk_tf else None},
         "kernel_ms": per_kernel,

@@ -98,6 +98,8 @@ def _declare(lib: ctypes.CDLL) -> None:
                                                       ctypes.POINTER(CbDims), _P]
     lib.cb_get_device_error.restype = ctypes.c_int
     lib.cb_get_device_error.argtypes = [_P]
+    lib.cb_pass_timestamps.restype = ctypes.c_int
+    lib.cb_pass_timestamps.argtypes = [_P, ctypes.POINTER(ctypes.c_uint64), _P]
     lib.cb_selftest_wait_timeout.restype = ctypes.c_int
     lib.cb_selftest_wait_timeout.argtypes = [ctypes.c_int32, _P, _P]
     lib.cb_copy_blocks.restype = ctypes.c_int
@@ -270,8 +272,8 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
     q [T, Hq, D] bf16; pages [P, bs, Hkv, D] bf16 (after the append); returns out [T, Hq, D]
     bf16, or (out, lse) when ``lse`` is True or an fp32 [T, Hq] tensor.  ``phase_events``:
     optional sequence of NUM_PHASE_EVENTS recorded torch.cuda.Event objects; the call records
-    them around its planner, decode and chunk kernels (see cb_options in cb.h).  ``serial``
-    runs the chunk kernel after the decode kernel instead of concurrently.  ``window`` > 0
+    them around its planner and its attention launch (see cb_options in cb.h).  ``serial``
+    runs the decode pass and the chunk pass as two launches instead of one.  ``window`` > 0
     selects sliding-window attention over the last ``window`` keys of each query.
     """
     import torch
@@ -330,7 +332,7 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
 def append_attention(q, k_new, v_new, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
                      block_size, scale, **kwargs):
     """kv_append then ragged_paged_attention in one call (cb_append_attention): same results,
-    with the attention planner overlapping the append.  Keyword arguments as for
+    with the append and the attention planner in one launch.  Keyword arguments as for
     ragged_paged_attention."""
     return ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens,
                                   block_size, scale, k_new=k_new, v_new=v_new, **kwargs)
@@ -343,3 +345,12 @@ def get_device_error(stream=None) -> int:
 
 def check_device_error(stream=None) -> None:
     _check(get_device_error(stream), "device")
+
+
+def pass_timestamps(workspace, stream=None) -> tuple[int, int, int, int]:
+    """%globaltimer stamps (ns) of the last attention call on `workspace`: first start and last
+    end of the decode pass, then of the chunk pass (0, 0 for a pass without work).  Waits for
+    the stream."""
+    ts = (ctypes.c_uint64 * 4)()
+    _check(library().cb_pass_timestamps(_ptr(workspace), ts, _stream(stream)), "cb_pass_timestamps")
+    return tuple(int(x) for x in ts)

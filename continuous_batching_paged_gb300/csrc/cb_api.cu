@@ -36,12 +36,6 @@ struct DeviceState {
   bool ready = false;
   int sm_count = 0;
   uint32_t* err = nullptr;
-  cudaStream_t aux = nullptr;      // second stream for the chunk kernel (created once)
-  cudaEvent_t ev_fork = nullptr;   // timing-free fork / join events (created once)
-  cudaEvent_t ev_join = nullptr;
-  cudaEvent_t ev_plan = nullptr;   // fused append + attention: planner done, append done
-  cudaEvent_t ev_append = nullptr;
-  std::mutex launch_mu;            // one fork/join sequence at a time per device
 };
 
 constexpr int kMaxDevices = 64;
@@ -69,12 +63,6 @@ cb_status device_state(DeviceState** out) {
     e = cudaGetSymbolAddress(&p, g_cb_error_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     st.err = static_cast<uint32_t*>(p);
-    e = cudaStreamCreateWithFlags(&st.aux, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_join, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_plan, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.ev_append, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "creating the library's stream and events");
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -208,9 +196,9 @@ cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void
   return CB_OK;
 }
 
-// The attention pass; with `app` non-NULL the KV-append of the same step is launched in the
-// same sequence, on the caller's stream while the planner (which reads only the metadata) runs
-// on the second stream, and both attention kernels wait for both.
+// The attention pass on `stream`: the planner, then the attention kernel (decode and chunk
+// passes in one launch); with `app` non-NULL the KV-append of the same step shares the
+// planner's launch.
 static cb_status attention(const void* q, const void* k_pages, const void* v_pages,
                            const int32_t* block_table, const int32_t* cu_seqlens_q,
                            const int32_t* kv_lens, int32_t block_size, float scale, void* out,
@@ -272,81 +260,77 @@ static cb_status attention(const void* q, const void* k_pages, const void* v_pag
   if (a.window < 0) return fail(CB_ERR_INVALID_ARG, "window must be >= 0, got %d", a.window);
   a.scale_log2 = scale * 1.4426950408889634f;
 
-  CUtensorMap qmap, kmap, vmap, kmap_c, vmap_c;
+  cb::AttnMaps maps;
   const uint64_t D = (uint64_t)a.D;
   const uint64_t rows = (uint64_t)a.P * (uint64_t)block_size;
   // Decode pass: dims (d, token, head) so one box {64, KB tokens, up to 8 heads} lands in shared
   // memory as [head][token] rows; chunk pass: dims (d, head, token), box {64, 1 head, KBp tokens}.
   const uint32_t HB = (uint32_t)(Hkv < cb::kMaxDecodeHeadsPerCta ? Hkv : cb::kMaxDecodeHeadsPerCta);
-  if ((st = encode_map(&kmap, k_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
-  if ((st = encode_map(&vmap, v_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
-  if ((st = encode_map(&kmap_c, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
-  if ((st = encode_map(&vmap_c, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
-  if ((st = encode_map(&qmap, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 1, 128)) != CB_OK) return st;
+  if ((st = encode_map(&maps.k_dec, k_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
+  if ((st = encode_map(&maps.v_dec, v_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
+  if ((st = encode_map(&maps.k_chunk, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
+  if ((st = encode_map(&maps.v_chunk, v_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
+  if ((st = encode_map(&maps.q, q, D, Hq, (uint64_t)a.T, D * 2, D * 2 * Hq, 1, 128)) != CB_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* const* ev = options != nullptr ? options->phase_events : nullptr;
   const bool serial = options != nullptr && (options->flags & CB_OPT_SERIAL);
-  auto mark = [&](int i, cudaStream_t on) -> cudaError_t {
-    return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), on) : cudaSuccess;
+  auto mark = [&](int i) -> cudaError_t {
+    return ev != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
-  std::lock_guard<std::mutex> lk(ds->launch_mu);
   cudaError_t e = cudaSuccess;
-  cudaStream_t cs = serial ? s : ds->aux;  // chunk kernel's stream
-  cudaStream_t dstr = s;                   // decode kernel's stream
-  if (app != nullptr && !serial) {
-    // Fork before the append: the planner runs on the second stream beside the append on the
-    // caller's.  The decode kernel then follows the planner on the second stream and the chunk
-    // kernel the append on the caller's, each after waiting for the other's predecessor: the
-    // stream that waits on the append's completion is the one whose next launch reaches the
-    // SMs first, and the decode kernel must place its CTAs first.
-    cs = s;
-    dstr = ds->aux;
-    cb::AppendArgs ap = *app;
+  cb::AppendArgs ap;
+  if (app != nullptr) {
+    ap = *app;
     ap.err = ds->err;
-    if ((e = cudaEventRecord(ds->ev_fork, s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(ds->aux, ds->ev_fork, 0)) != cudaSuccess)
-      return cuda_fail(e, "fork to the second stream");
-    if ((e = mark(0, ds->aux)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-    if ((e = cb::launch_plan(a, ds->aux)) != cudaSuccess) return cuda_fail(e, "plan launch");
-    if ((e = cudaEventRecord(ds->ev_plan, ds->aux)) != cudaSuccess)
-      return cuda_fail(e, "cudaEventRecord(plan)");
-    if ((e = cb::launch_kv_append(ap, s)) != cudaSuccess) return cuda_fail(e, "kv_append launch");
-    if ((e = cudaStreamWaitEvent(s, ds->ev_plan, 0)) != cudaSuccess ||
-        (e = cudaEventRecord(ds->ev_append, s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(ds->aux, ds->ev_append, 0)) != cudaSuccess)
-      return cuda_fail(e, "append / planner join");
-    if ((e = mark(1, ds->aux)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  }
+  if (app != nullptr && !serial) {
+    // One launch appends the step's K/V rows and plans the attention pass (which reads only
+    // the metadata, not the pages).
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+    if ((e = cb::launch_append_plan(ap, a, s)) != cudaSuccess) return cuda_fail(e, "append + plan launch");
   } else {
-    if (app != nullptr) {
-      cb::AppendArgs ap = *app;
-      ap.err = ds->err;
-      if ((e = cb::launch_kv_append(ap, s)) != cudaSuccess) return cuda_fail(e, "kv_append launch");
-    }
-    e = mark(0, s);
-    if (e == cudaSuccess && (e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
-    if (e == cudaSuccess) e = mark(1, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-    if (!serial) {
-      // fork: the chunk kernel's stream waits for the planner
-      if ((e = cudaEventRecord(ds->ev_fork, s)) != cudaSuccess ||
-          (e = cudaStreamWaitEvent(ds->aux, ds->ev_fork, 0)) != cudaSuccess)
-        return cuda_fail(e, "fork to the chunk stream");
-    }
+    if (app != nullptr && (e = cb::launch_kv_append(ap, s)) != cudaSuccess)
+      return cuda_fail(e, "kv_append launch");
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+    if ((e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
   }
-  if ((e = cb::launch_decode(a, kmap, vmap, dstr)) != cudaSuccess) return cuda_fail(e, "decode launch");
-  if ((e = mark(2, dstr)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-  if ((e = mark(3, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-  if ((e = cb::launch_prefill(a, qmap, kmap_c, vmap_c, cs)) != cudaSuccess)
-    return cuda_fail(e, "prefill launch");
-  if ((e = mark(4, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-  if (!serial) {
-    // join: work queued on the caller's stream after this call waits for the kernel on the
-    // second stream
-    if ((e = cudaEventRecord(ds->ev_join, ds->aux)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s, ds->ev_join, 0)) != cudaSuccess)
-      return cuda_fail(e, "join from the chunk stream");
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  const int head_groups = (Hkv + cb::kMaxDecodeHeadsPerCta - 1) / cb::kMaxDecodeHeadsPerCta;
+  if (serial) {
+    cb::AttnArgs d = a;
+    d.decode_grid = a.decode_ctas * head_groups;
+    d.prefill_ctas = 0;
+    if ((e = cb::launch_attention(d, maps, s)) != cudaSuccess) return cuda_fail(e, "attention launch");
+    if ((e = mark(2)) != cudaSuccess || (e = mark(3)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventRecord(phase event)");
+    cb::AttnArgs c = a;
+    c.decode_grid = 0;
+    if ((e = cb::launch_attention(c, maps, s)) != cudaSuccess) return cuda_fail(e, "attention launch");
+    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+  } else {
+    a.decode_grid = a.decode_ctas * head_groups;
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
+    if ((e = cb::launch_attention(a, maps, s)) != cudaSuccess) return cuda_fail(e, "attention launch");
+    if ((e = mark(2)) != cudaSuccess || (e = mark(4)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventRecord(phase event)");
   }
+  return CB_OK;
+}
+
+cb_status cb_pass_timestamps(const void* workspace, uint64_t* ts_ns, void* stream) {
+  t_last_error.clear();
+  if (workspace == nullptr || ts_ns == nullptr) return fail(CB_ERR_INVALID_ARG, "null pointer argument");
+  cb::PlanHeader h;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the plan header");
+  const bool dec = h.t_dec_end != 0, pf = h.t_pf_end != 0;
+  ts_ns[0] = dec ? h.t_dec_start : 0;
+  ts_ns[1] = dec ? h.t_dec_end : 0;
+  ts_ns[2] = pf ? h.t_pf_start : 0;
+  ts_ns[3] = pf ? h.t_pf_end : 0;
   return CB_OK;
 }
 

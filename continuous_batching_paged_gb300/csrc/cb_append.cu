@@ -18,17 +18,19 @@ namespace cb {
 constexpr int kAppendThreads = 256;
 constexpr int kAppendMaxChunks = 8;  // 16-byte chunks per lane and tensor in flight
 
-__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a) {
+// Tokens handled by warps first_warp, first_warp + nwarps, ...  kMaxChunks: 16-byte chunks per
+// lane and tensor in flight (registers: 8 per chunk pair).
+template <int kMaxChunks>
+__device__ __forceinline__ void append_tokens(const AppendArgs& a, int first_warp, int nwarps) {
   const int lane = threadIdx.x & 31;
   const int cpr = a.Hkv * a.D / 8;  // 16-byte chunks per token row
   const uint4* kn = static_cast<const uint4*>(a.k_new);
   const uint4* vn = static_cast<const uint4*>(a.v_new);
   uint4* kp = static_cast<uint4*>(a.k_pages);
   uint4* vp = static_cast<uint4*>(a.v_pages);
-  const int nwarps = gridDim.x * (kAppendThreads / 32);
   // Rows at or past cu_seqlens_q[S] are padding of the token tensors: left untouched.
   const int t_end = min(a.T, __ldg(a.cu_seqlens_q + a.S));
-  for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < t_end; t += nwarps) {
+  for (int t = first_warp; t < t_end; t += nwarps) {
     // Sequence of token t: the last s with cu[s] <= t (cu is non-decreasing).  Each round
     // probes 32 increasing positions in (lo, hi]; the lanes whose probe is <= t form a prefix.
     int lo = 0, hi = a.S;
@@ -74,10 +76,10 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a)
     const uint4* vs = vn + (size_t)t * cpr;
     uint4* kd = kp + (size_t)slot * cpr;
     uint4* vd = vp + (size_t)slot * cpr;
-    for (int base = 0; base < cpr; base += 32 * kAppendMaxChunks) {
-      uint4 kr[kAppendMaxChunks], vr[kAppendMaxChunks];
+    for (int base = 0; base < cpr; base += 32 * kMaxChunks) {
+      uint4 kr[kMaxChunks], vr[kMaxChunks];
 #pragma unroll
-      for (int i = 0; i < kAppendMaxChunks; ++i) {
+      for (int i = 0; i < kMaxChunks; ++i) {
         const int c = base + lane + 32 * i;
         if (c < cpr) {
           kr[i] = __ldg(ks + c);
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a)
         }
       }
 #pragma unroll
-      for (int i = 0; i < kAppendMaxChunks; ++i) {
+      for (int i = 0; i < kMaxChunks; ++i) {
         const int c = base + lane + 32 * i;
         if (c < cpr) {
           kd[c] = kr[i];
@@ -94,6 +96,11 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a)
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a) {
+  append_tokens<kAppendMaxChunks>(a, blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5),
+                                  gridDim.x * (kAppendThreads / 32));
 }
 
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
@@ -225,7 +232,7 @@ __device__ int pf_unit_bin(const AttnArgs& a, const int32_t* pf_seq, const int32
 // shared memory as well, so its binary searches cost no global round trips.
 constexpr int kPlanSmemSeqs = 2048;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
+__device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   static_assert(kCostBins == kPlanThreads, "one histogram bin per planner thread");
   __shared__ int sw[32][4];
   __shared__ int32_t s_dec_prefix[kPlanSmemSeqs + 1], s_pf_prefix[kPlanSmemSeqs + 1];
@@ -315,6 +322,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
     hdr->n_pf = n_pf;
     hdr->pf_qtiles = n_units;
     hdr->pf_counter = 0;
+    hdr->t_dec_start = hdr->t_pf_start = ~0ull;
+    hdr->t_dec_end = hdr->t_pf_end = 0ull;
   }
   __syncthreads();
   // Chunk units longest first (a counting sort on the K/V tiles each streams, descending), so
@@ -389,8 +398,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
   }
 }
 
+// Both planner launches let the attention kernel that follows them on the stream start early
+// (it is launched as their programmatic dependent and waits for their completion itself).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
+  allow_dependent_launch();
+  plan_cta(a);
+}
+
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// CTA 0 plans the attention pass (it reads only the metadata); CTAs 1.. append this step's
+// K/V rows, one warp per token, 32 tokens per CTA at a time.
+constexpr int kAppendPlanMaxChunks = 4;  // fits the 64 registers of a 1024-thread CTA
+__global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs ap, AttnArgs a) {
+  allow_dependent_launch();
+  if (blockIdx.x == 0) {
+    plan_cta(a);
+  } else {
+    constexpr int kWarps = kPlanThreads / 32;
+    append_tokens<kAppendPlanMaxChunks>(ap, (blockIdx.x - 1) * kWarps + (threadIdx.x >> 5),
+                                        (gridDim.x - 1) * kWarps);
+  }
+}
+
+cudaError_t launch_append_plan(const AppendArgs& ap, const AttnArgs& a, cudaStream_t stream) {
+  constexpr int kWarps = kPlanThreads / 32;
+  long long blocks = ((long long)ap.T + kWarps - 1) / kWarps;
+  if (blocks > 2048) blocks = 2048;
+  if (blocks < 1) blocks = 1;
+  append_plan_kernel<<<(unsigned)(1 + blocks), kPlanThreads, 0, stream>>>(ap, a);
   return cudaGetLastError();
 }
 

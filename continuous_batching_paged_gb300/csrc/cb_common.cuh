@@ -37,6 +37,13 @@ __host__ __device__ inline int window_first_key(int p, int window) {
   return (window > 0 && p >= window) ? p - window + 1 : 0;
 }
 
+// %globaltimer (ns since an arbitrary origin, the same on every SM).
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Workspace header (int32 words).
 struct PlanHeader {
   int32_t n_dec;          // number of decode sequences (q_len == 1)
@@ -45,7 +52,10 @@ struct PlanHeader {
   int32_t pf_qtiles;      // total work units over all chunk sequences (pf_unit_tiles)
   int32_t pf_counter;     // dynamic work counter of the prefill pass (reset by the planner)
   int32_t decode_ctas;    // CTAs the decode pass was planned for
-  int32_t pad[10];
+  int32_t pad[2];
+  // %globaltimer stamps (ns) of the attention kernel's roles, reset by the planner: first
+  // start and last end of the decode CTAs that had work, and of the chunk CTAs.
+  unsigned long long t_dec_start, t_dec_end, t_pf_start, t_pf_end;
 };
 
 // Byte offsets of the workspace sections (all 256-byte aligned).

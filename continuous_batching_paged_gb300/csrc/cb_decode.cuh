@@ -20,6 +20,8 @@
 //
 // Online softmax: for each new tile, m' = max(m, max_j x_j), rescale (l, o) by 2^(m - m'),
 // then add 2^(x_j - m') and 2^(x_j - m') v_j; x_j = scale * log2(e) * q.k_j.
+#pragma once
+
 #include "cb_common.cuh"
 #include "cb_launch.h"
 
@@ -396,12 +398,14 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
   }
 }
 
+// One CTA of the decode pass: CTA `bx` of the a.decode_ctas CTAs of KV-head group `hg`
+// (8 KV heads per group).  Runs in the attention kernel (cb_attention.cu) with that kernel's
+// dynamic shared memory; uses 32 * (HB + 1) of its threads.
 template <int D, int NTH>
-__global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
-    decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap) {
+__device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap* kmap,
+                                           const CUtensorMap* vmap, uint8_t* smem_raw, int bx,
+                                           int hg) {
   using SM = DecodeSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -411,7 +415,6 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
 
   const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hg = blockIdx.y;
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
   const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
   const int32_t* cta_first = reinterpret_cast<const int32_t*>(a.ws + L.cta_first);
 
   const long long ntiles = hdr->dec_tiles;
-  const int N = hdr->decode_ctas;  // planner's CTA count: <= gridDim.x, every range non-empty
+  const int N = hdr->decode_ctas;  // planner's CTA count: <= a.decode_ctas, every range non-empty
   // With N below the grid size the working CTAs are spread evenly over the grid, in pairs of
   // consecutive CTAs where N and the grid are even: CTA b (or pair b/2) works when it is the
   // first with its value of floor(b N / grid), and takes that value's range.  The block
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
   // Measured beside a chunk pass: with the first N CTAs working the decode pass ran ~6% slower;
   // with single CTAs spread, decode and chunk CTAs shared TPCs and the chunk pass ran ~5%
   // slower; spread pairs ran both at the speed of a launch of exactly N CTAs.
-  const int grid = (int)gridDim.x, bx = (int)blockIdx.x;
+  const int grid = a.decode_ctas;
   int c = bx;
   if (N < grid) {
     const bool pairs = ((N | grid) & 1) == 0;
@@ -452,8 +455,8 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
   if (warp == HB) {
     // ===================================================================== producer warp
     if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(kmap);
+      tma_prefetch_desc(vmap);
     }
     const int KB = a.KB;
     const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
@@ -530,9 +533,9 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
             const uint32_t off = (uint32_t)(lane * HB * KB * 128);  // run sb: [HB heads][KB keys]
 #pragma unroll
             for (int half = 0; half < SM::kHalves; ++half) {
-              tma_load_3d_hint(kst + half * SM::kHalfBytes + off, &kmap, bar_full + 8 * stage,
+              tma_load_3d_hint(kst + half * SM::kHalfBytes + off, kmap, bar_full + 8 * stage,
                                half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
-              tma_load_3d_hint(vst + half * SM::kHalfBytes + off, &vmap, bar_full + 8 * stage,
+              tma_load_3d_hint(vst + half * SM::kHalfBytes + off, vmap, bar_full + 8 * stage,
                                half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
             }
           }
@@ -545,50 +548,6 @@ __global__ void __launch_bounds__(32 * (kMaxDecodeHeadsPerCta + 1), 1)
     decode_consume<D, NTH>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
                            L, lane);
   }
-}
-
-template <int D>
-static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, cudaStream_t stream) {
-  using SM = DecodeSmem<D>;
-  static int configured_device = -1;
-  static int top_priority = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, 1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SM::kTotal);
-    int least = 0, greatest = 0;
-    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-    if (e != cudaSuccess) return e;
-    top_priority = greatest;
-    configured_device = dev;
-  }
-  const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
-  // The decode kernel runs at the highest launch priority: when it and the chunk kernel become
-  // ready together, the block scheduler places the decode CTAs first and the chunk kernel's
-  // persistent CTAs take the SMs the planner left free.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributePriority;
-  attr[0].val.priority = top_priority;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.decode_ctas, (a.Hkv + kMaxDecodeHeadsPerCta - 1) / kMaxDecodeHeadsPerCta);
-  cfg.blockDim = dim3(32 * (HB + 1));
-  cfg.dynamicSmemBytes = SM::kTotal;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (a.G <= 8) return cudaLaunchKernelEx(&cfg, decode_kernel<D, 1>, a, kmap, vmap);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, 2>, a, kmap, vmap);
-}
-
-cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream) {
-  if (a.D == 128) return launch_decode_d<128>(a, kmap, vmap, stream);
-  return launch_decode_d<64>(a, kmap, vmap, stream);
 }
 
 }  // namespace cb

@@ -31,9 +31,11 @@ struct AttnArgs {
   int S, T, Hq, Hkv, G, D, bs, max_blocks, P;
   int KB;              // rows per TMA box on the page pool, decode pass: gcd(bs, 16)
   int KBp;             // rows per TMA box on the page pool, chunk pass: gcd(bs, 128)
-  int decode_ctas;     // CTAs of the decode pass (<= CB_MAX_DECODE_CTAS)
+  int decode_ctas;     // CTAs of the decode pass per KV-head group (<= CB_MAX_DECODE_CTAS)
+  int decode_grid;     // decode-role CTAs of this attention launch (decode_ctas x head groups;
+                       // 0 when the launch runs the chunk pass only)
   int decode_auto;     // 1: the planner picks how many of them work (decode / chunk balance)
-  int prefill_ctas;    // persistent CTAs of the prefill pass
+  int prefill_ctas;    // persistent CTAs of the chunk pass (0 when the launch runs decode only)
   int window;          // > 0: query at position p sees keys (p - window, p]; 0: all <= p
   float scale_log2;    // softmax scale * log2(e)
 };
@@ -56,9 +58,15 @@ cudaError_t launch_block_move(const BlockMoveArgs& a, int sm_count, cudaStream_t
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, uint64_t* waited_ns,
                                  cudaStream_t stream);
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
-cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream);
-cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream);
+// The append of a step and the planner of its attention pass in one launch (CTA 0 plans, the
+// other CTAs append).
+cudaError_t launch_append_plan(const AppendArgs& ap, const AttnArgs& a, cudaStream_t stream);
+// Tensor maps of the attention pass: Q, and the page pools as the decode pass reads them
+// (box of a page run of all KV heads of a group) and as the chunk pass reads them (one head).
+struct AttnMaps {
+  CUtensorMap q, k_dec, v_dec, k_chunk, v_chunk;
+};
+// The attention kernel: a.decode_grid decode-role CTAs, then a.prefill_ctas chunk-role CTAs.
+cudaError_t launch_attention(const AttnArgs& a, const AttnMaps& maps, cudaStream_t stream);
 
 }  // namespace cb

@@ -30,6 +30,8 @@
 //               only when m grows by more than 8 in log2 units (otherwise the stale max keeps
 //               every p <= 2^8, exact enough in fp32 and bf16), and writes O / l as bf16.
 // TMEM columns: [0,128) S/P of A, [128,256) S/P of B, [256,256+D) O of A, then O of B.
+#pragma once
+
 #include "cb_common.cuh"
 #include "cb_launch.h"
 
@@ -131,14 +133,14 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
 
 // kWin: sliding-window attention (a.window > 0).  The full causal pass is compiled without
 // the window's bookkeeping, so it runs exactly the code it ran before windows existed.
+// One persistent CTA of the chunk pass (all kPrefillThreads threads).  Runs in the attention
+// kernel (cb_attention.cu) with that kernel's dynamic shared memory.
 template <int D, bool kWin>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
-    prefill_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                   const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap) {
+__device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap* qmap,
+                                            const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                            uint8_t* smem_raw) {
   using SM = PrefillSmem<D>;
   constexpr int NS = SM::kStages;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (warp == 0) {
       // =================================================================== TMA producer
       if (lane == 0) {
-        tma_prefetch_desc(&qmap);
-        tma_prefetch_desc(&kmap);
-        tma_prefetch_desc(&vmap);
+        tma_prefetch_desc(qmap);
+        tma_prefetch_desc(kmap);
+        tma_prefetch_desc(vmap);
       }
       const int KB = a.KBp;
       const int nsb = kChunkKeys / KB;  // page-run boxes per K/V tile (<= 128)
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           if (!mbar_wait(bar(SM::bItemEmpty + slot), ((k >> 1) & 1) ^ 1)) report(a.err, kErrTimeout);
           item = atomicAdd(&hdr->pf_counter, 1);
           if (item >= n_items) item = -1;
+          if (k == 0 && item >= 0) atomicMin(&hdr->t_pf_start, global_ns());  // role span
           item_ids[slot] = item;
           mbar_arrive(bar(SM::bItemFull + slot));
         }
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           for (int t = 0; t < (it.hasB ? 2 : 1); ++t)
 #pragma unroll
             for (int half = 0; half < SM::kHalves; ++half)
-              tma_load_3d(sbase + SM::kQ0 + t * SM::kQTile + half * SM::kQHalf, &qmap,
+              tma_load_3d(sbase + SM::kQ0 + t * SM::kQTile + half * SM::kQHalf, qmap,
                           bar(SM::bQFull), half * 64, it.head[t], it.tok[t]);
         }
         const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
                 for (int half = 0; half < SM::kHalves; ++half)
                   tma_load_3d((kv ? vst : kst) + half * SM::kKVHalf + sb * KB * 128,
-                              kv ? &vmap : &kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
+                              kv ? vmap : kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
                               half * 64, it.kvh, token);
               }
             }
@@ -533,6 +536,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       if (store && a.lse != nullptr)
         a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head[t]] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+      if (r == 0) atomicMax(&hdr->t_pf_end, global_ns());  // role span: last item's end
       tc_fence_before();
       mbar_arrive(bar(SM::bOFree + t));
       gx += nt - it.j0;
@@ -546,34 +550,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-template <int D, bool kWin>
-static cudaError_t launch_prefill_d(const AttnArgs& a, const CUtensorMap& qmap,
-                                    const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                    cudaStream_t stream) {
-  using SM = PrefillSmem<D>;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWin>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  prefill_kernel<D, kWin><<<a.prefill_ctas, kPrefillThreads, SM::kTotal, stream>>>(a, qmap, kmap, vmap);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream) {
-  if (a.window > 0) {
-    if (a.D == 128) return launch_prefill_d<128, true>(a, qmap, kmap, vmap, stream);
-    return launch_prefill_d<64, true>(a, qmap, kmap, vmap, stream);
-  }
-  if (a.D == 128) return launch_prefill_d<128, false>(a, qmap, kmap, vmap, stream);
-  return launch_prefill_d<64, false>(a, qmap, kmap, vmap, stream);
 }
 
 }  // namespace cb

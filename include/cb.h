@@ -127,13 +127,14 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
  *   decode_ctas   number of CTAs the decode pass spreads its key tiles over (0 = one per SM;
  *                 1 forces every decode sequence into a single unsplit pass).  Results for
  *                 different values agree within rounding; at most CB_MAX_DECODE_CTAS.
- *   flags         CB_OPT_SERIAL: run the chunk kernel after the decode kernel on `stream`
- *                 instead of concurrently on the library's second stream.
+ *   flags         CB_OPT_SERIAL: run the decode pass and then the chunk pass as two launches
+ *                 instead of together in one.
  *   phase_events  NULL, or an array of CB_NUM_PHASE_EVENTS cudaEvent_t (created by the
- *                 caller, passed as void*).  The call records [0] on `stream` before the
- *                 planner, [1] after it, [2] after the decode kernel (which also merges split
- *                 sequences), and [3] / [4] just before / after the chunk kernel on the stream
- *                 that runs it, so cudaEventElapsedTime gives each kernel's device time.
+ *                 caller, passed as void*), all recorded on `stream`: [0] before the planner,
+ *                 [1] after it, [2] after the decode pass (which also merges split sequences),
+ *                 [3] / [4] before / after the chunk pass.  With both passes in one launch
+ *                 (the default) [1] and [3] mark that launch's start and [2] and [4] its end;
+ *                 cb_pass_timestamps gives the two passes' own spans inside it.
  *   window        0: full causal attention.  W > 0: sliding-window attention, for models with
  *                 sliding-window layer groups (named in "Continuous batching in transformers",
  *                 paged-cache section, which does not define the mask; this is the common
@@ -141,10 +142,10 @@ cb_status cb_ragged_paged_attention(const void* q, const void* k_pages, const vo
  *                 p - W < j <= p, i.e. itself and the W - 1 keys before it.  Keys older than
  *                 the window are not read (neither pass streams them).
  *
- * Concurrency: by default the decode kernel (HBM-bound) runs on `stream` while the chunk kernel
- * (tensor-bound) runs on a second stream that the library creates once per device, forked from
- * and joined back into `stream` with events; the chunk kernel's CTAs take SMs as decode CTAs
- * finish.  Work the caller queues on `stream` after the call waits for both.
+ * Concurrency: everything runs on `stream`.  The decode pass (HBM-bound) and the chunk pass
+ * (tensor-bound) share one kernel launch: its first CTAs are the decode CTAs, which the block
+ * scheduler places first, and the chunk CTAs take the SMs the planner leaves free and then the
+ * SMs the decode CTAs free as they finish.
  */
 #define CB_NUM_PHASE_EVENTS 5
 #define CB_OPT_SERIAL 1
@@ -169,13 +170,12 @@ cb_status cb_ragged_paged_attention_ex(const void* q, const void* k_pages, const
 /*
  * cb_append_attention -- cb_kv_append followed by cb_ragged_paged_attention_ex in one call, with
  * the same arguments and the same results (bit for bit).  The attention pass's planner reads
- * only the metadata, so it runs on the library's second stream while the append runs on
- * `stream`; the decode and chunk kernels then wait for both (the decode kernel on the second
- * stream, the chunk kernel on `stream`).  This overlaps the two short launch-bound kernels
- * that begin every step.  Phase events: [0] / [1] on the second stream before the planner and
- * before the decode kernel, [2] after it; [3] / [4] around the chunk kernel on `stream`.  k_new / v_new as in cb_kv_append; every other
- * argument as in cb_ragged_paged_attention_ex (with CB_OPT_SERIAL the four kernels run one
- * after the other on `stream`).
+ * only the metadata, so one launch does both the append and the planning (one CTA plans while
+ * the others append), and the attention kernel follows: two launches per step, both on
+ * `stream`.  Phase events as in cb_ragged_paged_attention_ex, [0] before and [1] after the
+ * append + planner launch.  k_new / v_new as in cb_kv_append; every other argument as in
+ * cb_ragged_paged_attention_ex (with CB_OPT_SERIAL the append, the planner, the decode pass
+ * and the chunk pass are four launches, one after the other).
  */
 cb_status cb_append_attention(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                               const void* q, const int32_t* block_table,
@@ -183,6 +183,16 @@ cb_status cb_append_attention(const void* k_new, const void* v_new, void* k_page
                               int32_t block_size, float scale, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, const cb_dims* dims,
                               const cb_options* options, void* stream);
+
+/*
+ * cb_pass_timestamps -- device time stamps (%globaltimer, ns) of the two passes of the last
+ * attention call that used `workspace`: ts_ns[0] / [1] the first start and the last end of the
+ * decode CTAs that had work, ts_ns[2] / [3] the same for the chunk CTAs (the end is the last
+ * chunk item's output written); 0 / 0 for a pass that had no work.  Waits for `stream`, then
+ * reads 64 bytes of the workspace.  For profiling: inside one launch CUDA events cannot separate
+ * the passes.  Errors: CB_ERR_INVALID_ARG (NULL pointer), CB_ERR_CUDA.
+ */
+cb_status cb_pass_timestamps(const void* workspace, uint64_t* ts_ns, void* stream);
 
 /*
  * cb_ragged_paged_attention_noalloc -- cb_ragged_paged_attention without a workspace argument.

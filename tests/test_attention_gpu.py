@@ -307,3 +307,29 @@ def test_fused_append_attention_equals_separate_calls(cuda_lib, cfg, serial):
     assert torch.equal(out_a.view(torch.int16), out_f.view(torch.int16))
     assert torch.equal(a.k_pages.view(torch.int16), f.k_pages.view(torch.int16))
     assert torch.equal(a.v_pages.view(torch.int16), f.v_pages.view(torch.int16))
+
+
+@pytest.mark.parametrize("q_lens,kv_lens,has_dec,has_chunk", [
+    ([1, 1, 1, 1], [300, 40, 1000, 77], True, False),        # decode tokens only
+    ([200, 130], [900, 130], False, True),                   # chunks only
+    ([1, 140, 1, 1], [500, 400, 90, 2000], True, True),      # both passes in one launch
+])
+def test_pass_timestamps_mark_the_passes_that_ran(cuda_lib, q_lens, kv_lens, has_dec, has_chunk):
+    # the attention launch stamps the first start and last end of each pass that had work;
+    # a pass without work reports (0, 0)
+    b = workloads.build_batch(q_lens, kv_lens, 8, 2, 128, 16, seed=77, num_pages=600,
+                              max_blocks=160, shuffle_pages=True, name="stamps")
+    db = DeviceBatch(b)
+    db.append()
+    ws = torch.empty(cb.workspace_size(b.num_seqs, 8, 2, 128, b.num_pages, b.max_blocks, 16,
+                                       b.num_tokens), dtype=torch.uint8, device="cuda")
+    out = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
+                                    db.kv_lens, 16, b.scale, workspace=ws)
+    ts = cb.pass_timestamps(ws)
+    assert cb.get_device_error() == cb.CB_OK
+    assert (ts[0] < ts[1]) == has_dec and (ts[0] == ts[1] == 0) == (not has_dec)
+    assert (ts[2] < ts[3]) == has_chunk and (ts[2] == ts[3] == 0) == (not has_chunk)
+    kp, vp = oracle_append(b)
+    ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                        16, b.scale)
+    assert_close(out.float().cpu().numpy(), ref, "stamps batch")
