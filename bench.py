@@ -687,13 +687,15 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     step_ms = 0.0
+    per_step = []
     for _ in range(args.steps):
         flush_l2()
         ev_start.record()
         step(False)
         ev_end.record()
         ev_end.synchronize()
-        step_ms += ev_start.elapsed_time(ev_end)
+        per_step.append(ev_start.elapsed_time(ev_end))
+        step_ms += per_step[-1]
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
@@ -864,7 +866,10 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "step_ms_stats": {"median": statistics.median(per_step), "min": min(per_step),
+                          "max": max(per_step)},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(b, args),
         "e2e": {"value": world * b.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",

@@ -168,8 +168,13 @@ __device__ __forceinline__ void block_scan4(int v[4], int ex[4], int tot[4], int
 // before td it ends near W/M (plus a short longest-first tail); if not, the items still
 // unclaimed when decode ends each take a full item time on the newly free SMs, so the step is
 // td + (W - M td)/SMs + about half an item.  The choice is the largest N within 1% of the
-// modelled minimum, so that the decode pass keeps its bandwidth where the curve is flat.
-// Without chunk work all CTAs decode.  Called by one full warp; candidates
+// modelled minimum, so that the decode pass keeps its bandwidth where the curve is flat --
+// unless the minimum lies where the chunk pass is the longer one: there the model is flat in N
+// (decode SM time is about constant while it is not bandwidth-bound) and the measured step
+// is shortest with few decode CTAs that still finish early (chunk-heavy batch: N = 24..40
+// 0.307 ms, N = 56 0.314 ms), so the choice is the smallest N within 1% whose decode pass
+// takes at most a quarter of the step.  Without chunk work all CTAs decode.  Called by one
+// full warp; candidates
 // N = 4, 8, ... are spread over the lanes, in fp32 (the fp64 rate of this part is far too low
 // for even this much arithmetic on one thread).
 __device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int chunk_items,
@@ -182,25 +187,41 @@ __device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int chunk_
   const float item_us = w_us / (float)chunk_items;
   const float b_mb = dec_bytes * 1e-6f;             // decode bytes / 1e6: MB / (TB/s) = us
   const int n_cand = (cap + 3) / 4;
-  float t[4];
+  float t[4], td[4];
+  bool chunk_bound[4];
   int n[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = lane + 32 * k;
     n[k] = 4 * (i + 1) < cap ? 4 * (i + 1) : cap;
     t[k] = 3.4e38f;
+    td[k] = 0.f;
+    chunk_bound[k] = false;
     if (i < n_cand) {
       const float lin = 0.11f * n[k], sat = 6.8f;
       const float bw = rcbrtf(1.f / (lin * lin * lin) + 1.f / (sat * sat * sat));
-      const float td = b_mb / bw;
+      td[k] = b_mb / bw;
       const int m = max_ctas - n[k];
-      const float rest = w_us - (float)m * td;  // chunk work not done when decode ends
-      t[k] = rest <= 0.f ? fmaxf(td, w_us / (float)m + 0.15f * item_us)
-                         : td + rest / (float)max_ctas + 0.5f * item_us;
+      const float rest = w_us - (float)m * td[k];  // chunk work not done when decode ends
+      chunk_bound[k] = rest > 0.f;
+      t[k] = rest <= 0.f ? fmaxf(td[k], w_us / (float)m + 0.15f * item_us)
+                         : td[k] + rest / (float)max_ctas + 0.5f * item_us;
     }
   }
   float t_min = fminf(fminf(t[0], t[1]), fminf(t[2], t[3]));
   for (int o = 16; o > 0; o >>= 1) t_min = fminf(t_min, __shfl_xor_sync(0xffffffffu, t_min, o));
+  bool min_chunk_bound = false;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) min_chunk_bound |= (t[k] == t_min && chunk_bound[k]);
+  min_chunk_bound = __any_sync(0xffffffffu, min_chunk_bound);
+  if (min_chunk_bound) {
+    int small = cap + 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (t[k] <= 1.01f * t_min && td[k] <= 0.25f * t[k]) small = small < n[k] ? small : n[k];
+    for (int o = 16; o > 0; o >>= 1) small = min(small, __shfl_xor_sync(0xffffffffu, small, o));
+    if (small <= cap) return small;
+  }
   int best = 1;
 #pragma unroll
   for (int k = 0; k < 4; ++k)
@@ -211,17 +232,25 @@ __device__ int choose_decode_ctas(float dec_bytes, float chunk_flops, int chunk_
 
 // Histogram bin of chunk unit g (global index in chunk-sequence order): units that stream
 // more K/V tiles get lower bins, so an ascending walk over the bins is longest first.
+// With `lens` (shared memory: q_len and prior context of the i-th chunk sequence, interleaved)
+// the lengths need no global loads.
 __device__ int pf_unit_bin(const AttnArgs& a, const int32_t* pf_seq, const int32_t* pf_prefix,
-                           int n_pf, int g) {
+                           const int2* lens, int n_pf, int g) {
   int lo = 0, hi = n_pf - 1;  // largest i with pf_prefix[i] <= g
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (pf_prefix[mid] <= g) lo = mid; else hi = mid - 1;
   }
-  const int s = pf_seq[lo];
   const int u = g - pf_prefix[lo];
-  const int q_len = a.cu_seqlens_q[s + 1] - a.cu_seqlens_q[s];
-  const int ctx = a.kv_lens[s] - q_len;
+  int q_len, ctx;
+  if (lens != nullptr) {
+    q_len = lens[lo].x;
+    ctx = lens[lo].y;
+  } else {
+    const int s = pf_seq[lo];
+    q_len = a.cu_seqlens_q[s + 1] - a.cu_seqlens_q[s];
+    ctx = a.kv_lens[s] - q_len;
+  }
   const int rows = min((u + 1) * pf_unit_tiles(a.G) * kPrefillTileM, q_len);
   const int first = window_first_key(ctx + u * pf_unit_tiles(a.G) * kPrefillTileM, a.window);
   const int tiles = (ctx + rows + kChunkKeys - 1) / kChunkKeys - first / kChunkKeys;
@@ -237,6 +266,7 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   __shared__ int sw[32][4];
   __shared__ int32_t s_dec_prefix[kPlanSmemSeqs + 1], s_pf_prefix[kPlanSmemSeqs + 1];
   __shared__ int32_t s_pf_seq[kPlanSmemSeqs];
+  __shared__ int2 s_pf_lens[kPlanSmemSeqs];  // (q_len, prior context) of each chunk sequence
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
   int32_t* dec_seq = reinterpret_cast<int32_t*>(a.ws + L.dec_seq);
@@ -247,10 +277,6 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   const int tid = threadIdx.x;
   const long long max_kv = (long long)a.max_blocks * a.bs;
 
-  if (tid == 0) {
-    if (a.cu_seqlens_q[0] != 0 || a.cu_seqlens_q[a.S] > a.T) report(a.err, kErrOutOfRange);
-  }
-  __syncthreads();
   float my_keys = 0.f, my_pairs = 0.f;  // work estimates for the decode / chunk balance
   bool bad = false;
   const int unit_rows = pf_unit_tiles(a.G) * kPrefillTileM;
@@ -262,6 +288,7 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
       const int c0 = a.cu_seqlens_q[s], c1 = a.cu_seqlens_q[s + 1];
       const int q_len = c1 - c0;
       const int kv = a.kv_lens[s];
+      if (s == 0 && c0 != 0) report(a.err, kErrOutOfRange);  // cu_seqlens_q[0] must be 0
       const bool ok = c0 >= 0 && c1 <= a.T && q_len >= 0 && kv >= q_len && kv <= max_kv;
       if (!ok) {
         report(a.err, kErrOutOfRange);
@@ -302,6 +329,8 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
       if (i < kPlanSmemSeqs) {
         s_pf_seq[i] = s;
         s_pf_prefix[i] = carry[3] + ex[3];
+        const int q_len = a.cu_seqlens_q[s + 1] - a.cu_seqlens_q[s];
+        s_pf_lens[i] = make_int2(q_len, a.kv_lens[s] - q_len);
       }
     }
 #pragma unroll
@@ -338,15 +367,16 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
     const bool pf_local = n_pf <= kPlanSmemSeqs;
     const int32_t* ps = pf_local ? s_pf_seq : pf_seq;
     const int32_t* pp = pf_local ? s_pf_prefix : pf_prefix;
+    const int2* lens = pf_local ? s_pf_lens : nullptr;
     for (int g = tid; g < n_units; g += kPlanThreads)
-      atomicAdd(&hist[pf_unit_bin(a, ps, pp, n_pf, g)], 1);
+      atomicAdd(&hist[pf_unit_bin(a, ps, pp, lens, n_pf, g)], 1);
     __syncthreads();
     int v[4] = {hist[tid], 0, 0, 0}, ex[4], tot[4];
     block_scan4(v, ex, tot, sw);
     hist[tid] = ex[0];
     __syncthreads();
     for (int g = tid; g < n_units; g += kPlanThreads)
-      pf_order[atomicAdd(&hist[pf_unit_bin(a, ps, pp, n_pf, g)], 1)] = g;
+      pf_order[atomicAdd(&hist[pf_unit_bin(a, ps, pp, lens, n_pf, g)], 1)] = g;
   }
   // First decode sequence of each decode CTA: CTA c owns tiles [c*n/N, (c+1)*n/N), with N
   // capped at the tile count so that no CTA range is empty.
@@ -404,7 +434,7 @@ __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(AttnArgs a) {
   allow_dependent_launch();
   plan_cta(a);
 }
@@ -417,7 +447,7 @@ cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
 // CTA 0 plans the attention pass (it reads only the metadata); CTAs 1.. append this step's
 // K/V rows, one warp per token, 32 tokens per CTA at a time.
 constexpr int kAppendPlanMaxChunks = 4;  // fits the 64 registers of a 1024-thread CTA
-__global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs ap, AttnArgs a) {
+__global__ void __launch_bounds__(kPlanThreads, 1) append_plan_kernel(AppendArgs ap, AttnArgs a) {
   allow_dependent_launch();
   if (blockIdx.x == 0) {
     plan_cta(a);

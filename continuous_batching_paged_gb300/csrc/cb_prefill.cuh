@@ -309,11 +309,14 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         if (elect_one()) tc_commit(b);
         __syncwarp();
       };
-      // S_t = Q_t K^T of K/V tile gg into tile t's S buffer.
-      auto issue_s = [&](int t, uint32_t gg) {
+      // S_t = Q_t K^T of K/V tile gg into tile t's S buffer.  `k_ready`: this thread already
+      // waited for K tile gg (the other tile's S product read it first).
+      auto issue_s = [&](int t, uint32_t gg, bool k_ready) {
         const int stage = gg % NS;
-        wait(bar(SM::bKFull + stage), (gg / NS) & 1);
-        tc_fence_after();
+        if (!k_ready) {
+          wait(bar(SM::bKFull + stage), (gg / NS) & 1);
+          tc_fence_after();
+        }
         const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kQTile) >> 4);
         const uint64_t kd = k_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
         if (elect_one()) {
@@ -340,7 +343,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         wait(bar(SM::bQFull), k & 1);
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (nt_t[t] > 0) issue_s(t, g);
+          if (nt_t[t] > 0) issue_s(t, g, t == 1 && nt_t[0] > 0);
         commit(bar(SM::bKEmpty + g % NS));
         for (int j = it.j0; j < it.nt_all && ok; ++j) {
           const uint32_t gj = g + (j - it.j0);
@@ -364,7 +367,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
               if (j == nt_t[t] - 1) tc_commit(bar(SM::bOFinal + t));
             }
             __syncwarp();
-            if (j + 1 < nt_t[t]) issue_s(t, gj + 1);
+            if (j + 1 < nt_t[t]) issue_s(t, gj + 1, t == 1 && j + 1 < nt_t[0]);
           }
           commit(bar(SM::bVEmpty + stage));
           if (j + 1 < it.nt_all) commit(bar(SM::bKEmpty + (gj + 1) % NS));
