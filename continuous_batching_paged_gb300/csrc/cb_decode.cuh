@@ -398,6 +398,110 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
   }
 }
 
+// The producer warp of a decode CTA (see decode_cta): walks the CTA's tile range and issues
+// the TMA copies of every tile's page runs into the stage ring.
+template <int D>
+__device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensorMap* kmap,
+                                               const CUtensorMap* vmap, uint32_t sbase,
+                                               uint32_t bar_full, uint32_t bar_empty,
+                                               StageInfo* info, const PlanHeader* hdr,
+                                               const int32_t* dec_seq, const int32_t* dec_prefix,
+                                               const int32_t* cta_first, int c, int hg, int HB,
+                                               long long t0, long long t1, int lane) {
+  using SM = DecodeSmem<D>;
+    // ===================================================================== producer warp
+  if (lane == 0) {
+    tma_prefetch_desc(kmap);
+    tma_prefetch_desc(vmap);
+  }
+  const int KB = a.KB;
+  const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
+  const uint64_t stream_policy = l2_policy_evict_first();  // each K/V row is read once
+  const int tiles_per_batch = 32 / nsb;
+  int d = cta_first[c];
+  long long t = t0;
+  long long it = 0;
+  bool abort = false;
+  while (t < t1 && !abort) {
+    if (d >= hdr->n_dec) { report(a.err, kErrOutOfRange); break; }
+    const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
+    const int s = dec_seq[d];
+    const int kv = a.kv_lens[s];
+    const int tok = a.cu_seqlens_q[s];
+    // with a sliding window the sequence's tiles start at the one holding its first key
+    const int lo_key = window_first_key(kv - 1, a.window);
+    const int first_tile_key = lo_key / kDecodeTileKeys * kDecodeTileKeys;
+    const long long lo = t > p0 ? t : p0;
+    const long long hi = t1 < p1 ? t1 : p1;
+    const bool complete = p0 >= t0 && p1 <= t1;
+    const int32_t* row = a.block_table + (size_t)s * a.max_blocks;
+    for (long long tb = lo; tb < hi && !abort; tb += tiles_per_batch) {
+      // Prefetch the block-table entries of up to 32 (tile, sub-box) pairs.
+      int entry = -1;
+      {
+        const long long tile = tb + lane / nsb;
+        const int pos = first_tile_key + (int)(tile - p0) * kDecodeTileKeys + (lane % nsb) * KB;
+        if (lane < tiles_per_batch * nsb && tile < hi && pos < kv) {
+          const int lb = pos / a.bs;
+          entry = lb < a.max_blocks ? __ldg(row + lb) : -2;
+        }
+      }
+      const int nb = (int)((hi - tb) < tiles_per_batch ? (hi - tb) : tiles_per_batch);
+      for (int tl = 0; tl < nb; ++tl, ++it) {
+        const long long tile = tb + tl;
+        const int stage = (int)(it % kDecodeStages);
+        const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+        if (lane == 0 && !mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
+          report(a.err, kErrTimeout);
+          abort = true;
+        }
+        abort = __shfl_sync(0xffffffffu, abort, 0);
+        if (abort) break;
+        const int key0 = first_tile_key + (int)(tile - p0) * kDecodeTileKeys;
+        // One TMA box per (page run sb, half of D, K or V) covers all HB heads of the run:
+        // lane sb handles run sb (nsb <= 16 runs per tile).
+        const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (lane < nsb ? lane : 0));
+        const int pos = key0 + lane * KB;
+        const bool want = lane < nsb && pos < kv;
+        const bool valid = want && e >= 0 && e < a.P;
+        if (want && !valid) report(a.err, kErrOutOfRange);
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        if (lane == 0) {
+          StageInfo& si = info[stage];
+          si.seq = s;
+          si.dec = d;
+          si.tok = tok;
+          si.kv = kv;
+          si.lo = lo_key;
+          si.key0 = key0;
+          si.p0 = (int)p0;
+          si.p1 = (int)p1;
+          si.flags = (tile == lo ? kInfoFirst : 0u) | (tile == hi - 1 ? kInfoLast : 0u) |
+                     (complete ? kInfoComplete : 0u);
+          mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                nvalid * (uint32_t)(2 * SM::kHalves * KB * HB * 128));
+        }
+        __syncwarp();
+        if (valid) {
+          const int token = e * a.bs + (pos % a.bs);
+          const uint32_t kst = sbase + stage * SM::kStageBytes;
+          const uint32_t vst = kst + SM::kKVBytes;
+          const uint32_t off = (uint32_t)(lane * HB * KB * 128);  // run sb: [HB heads][KB keys]
+#pragma unroll
+          for (int half = 0; half < SM::kHalves; ++half) {
+            tma_load_3d_hint(kst + half * SM::kHalfBytes + off, kmap, bar_full + 8 * stage,
+                             half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
+            tma_load_3d_hint(vst + half * SM::kHalfBytes + off, vmap, bar_full + 8 * stage,
+                             half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
+          }
+        }
+      }
+    }
+    t = hi;
+    ++d;
+  }
+}
+
 // One CTA of the decode pass: CTA `bx` of the a.decode_ctas CTAs of KV-head group `hg`
 // (8 KV heads per group).  Runs in the attention kernel (cb_attention.cu) with that kernel's
 // dynamic shared memory; uses 32 * (HB + 1) of its threads.
@@ -452,101 +556,30 @@ __device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap*
   }
   __syncthreads();
 
-  if (warp == HB) {
-    // ===================================================================== producer warp
-    if (lane == 0) {
-      tma_prefetch_desc(kmap);
-      tma_prefetch_desc(vmap);
-    }
-    const int KB = a.KB;
-    const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
-    const uint64_t stream_policy = l2_policy_evict_first();  // each K/V row is read once
-    const int tiles_per_batch = 32 / nsb;
-    int d = cta_first[c];
-    long long t = t0;
-    long long it = 0;
-    bool abort = false;
-    while (t < t1 && !abort) {
-      if (d >= hdr->n_dec) { report(a.err, kErrOutOfRange); break; }
-      const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
-      const int s = dec_seq[d];
-      const int kv = a.kv_lens[s];
-      const int tok = a.cu_seqlens_q[s];
-      // with a sliding window the sequence's tiles start at the one holding its first key
-      const int lo_key = window_first_key(kv - 1, a.window);
-      const int first_tile_key = lo_key / kDecodeTileKeys * kDecodeTileKeys;
-      const long long lo = t > p0 ? t : p0;
-      const long long hi = t1 < p1 ? t1 : p1;
-      const bool complete = p0 >= t0 && p1 <= t1;
-      const int32_t* row = a.block_table + (size_t)s * a.max_blocks;
-      for (long long tb = lo; tb < hi && !abort; tb += tiles_per_batch) {
-        // Prefetch the block-table entries of up to 32 (tile, sub-box) pairs.
-        int entry = -1;
-        {
-          const long long tile = tb + lane / nsb;
-          const int pos = first_tile_key + (int)(tile - p0) * kDecodeTileKeys + (lane % nsb) * KB;
-          if (lane < tiles_per_batch * nsb && tile < hi && pos < kv) {
-            const int lb = pos / a.bs;
-            entry = lb < a.max_blocks ? __ldg(row + lb) : -2;
-          }
-        }
-        const int nb = (int)((hi - tb) < tiles_per_batch ? (hi - tb) : tiles_per_batch);
-        for (int tl = 0; tl < nb; ++tl, ++it) {
-          const long long tile = tb + tl;
-          const int stage = (int)(it % kDecodeStages);
-          const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
-          if (lane == 0 && !mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
-            report(a.err, kErrTimeout);
-            abort = true;
-          }
-          abort = __shfl_sync(0xffffffffu, abort, 0);
-          if (abort) break;
-          const int key0 = first_tile_key + (int)(tile - p0) * kDecodeTileKeys;
-          // One TMA box per (page run sb, half of D, K or V) covers all HB heads of the run:
-          // lane sb handles run sb (nsb <= 16 runs per tile).
-          const int e = __shfl_sync(0xffffffffu, entry, tl * nsb + (lane < nsb ? lane : 0));
-          const int pos = key0 + lane * KB;
-          const bool want = lane < nsb && pos < kv;
-          const bool valid = want && e >= 0 && e < a.P;
-          if (want && !valid) report(a.err, kErrOutOfRange);
-          const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-          if (lane == 0) {
-            StageInfo& si = info[stage];
-            si.seq = s;
-            si.dec = d;
-            si.tok = tok;
-            si.kv = kv;
-            si.lo = lo_key;
-            si.key0 = key0;
-            si.p0 = (int)p0;
-            si.p1 = (int)p1;
-            si.flags = (tile == lo ? kInfoFirst : 0u) | (tile == hi - 1 ? kInfoLast : 0u) |
-                       (complete ? kInfoComplete : 0u);
-            mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                  nvalid * (uint32_t)(2 * SM::kHalves * KB * HB * 128));
-          }
-          __syncwarp();
-          if (valid) {
-            const int token = e * a.bs + (pos % a.bs);
-            const uint32_t kst = sbase + stage * SM::kStageBytes;
-            const uint32_t vst = kst + SM::kKVBytes;
-            const uint32_t off = (uint32_t)(lane * HB * KB * 128);  // run sb: [HB heads][KB keys]
-#pragma unroll
-            for (int half = 0; half < SM::kHalves; ++half) {
-              tma_load_3d_hint(kst + half * SM::kHalfBytes + off, kmap, bar_full + 8 * stage,
-                               half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
-              tma_load_3d_hint(vst + half * SM::kHalfBytes + off, vmap, bar_full + 8 * stage,
-                               half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
-            }
-          }
-        }
-      }
-      t = hi;
-      ++d;
-    }
-  } else if (warp < HB) {
+  auto produce = [&]() {
+    decode_produce<D>(a, kmap, vmap, sbase, bar_full, bar_empty, info, hdr, dec_seq, dec_prefix,
+                      cta_first, c, hg, HB, t0, t1, lane);
+  };
+  auto consume = [&]() {
     decode_consume<D, NTH>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
                            L, lane);
+  };
+  if constexpr (NTH == 2) {
+    // Up to 16 query heads per warp need more than the launch's 168 registers per thread:
+    // warpgroups 0 and 1 (the consumers, and the producer when HB < 8) take 200, warpgroup 2
+    // (the producer when HB = 8, and idle warps) gives up to 104; 2 x 128 x 200 + 128 x 104 =
+    // 384 x 168.  Each role runs inside the branch that set its register count.
+    if (warp < 8) {
+      regs_inc<200>();
+      if (warp == HB) produce();
+      else if (warp < HB) consume();
+    } else {
+      regs_dec<104>();
+      if (warp == HB) produce();
+    }
+  } else {
+    if (warp == HB) produce();
+    else if (warp < HB) consume();
   }
 }
 
