@@ -358,8 +358,9 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   // Chunk units longest first (a counting sort on the K/V tiles each streams, descending), so
   // that the chunk CTAs, taking items in this order from a shared counter, schedule them
   // longest-processing-time first.  Units of equal cost land in any order: each item writes
-  // its own output rows, so the order never changes a result.
-  {
+  // its own output rows, so the order never changes a result.  (n_units is the same in every
+  // thread, so a batch without chunk work skips the section, barriers included.)
+  if (n_units > 0) {
     __shared__ int hist[kCostBins];
     int32_t* pf_order = reinterpret_cast<int32_t*>(a.ws + L.pf_order);
     hist[tid] = 0;
