@@ -301,13 +301,41 @@ def cpu_sample_plan(b: workloads.Batch, budget_s: float):
         n = min(len(order), max(n + 1, int(n * min(4.0, budget_s / max(dt, 1e-3)))))
 
 
+_ONE_THREAD = """
+import pickle, sys, time
+sys.path.insert(0, sys.argv[1])
+import bench
+from oracle import paged_attention  # noqa: F401  (imported before the clock starts)
+sb = pickle.load(sys.stdin.buffer)
+t0 = time.perf_counter()
+bench.oracle_step(sb)
+print(time.perf_counter() - t0)
+"""
+
+
+def oracle_seconds_one_thread(sb: workloads.Batch):
+    """The same oracle pass in a child process whose BLAS / OpenMP pools have one thread."""
+    import pickle
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT], input=pickle.dumps(sb),
+                           capture_output=True, env=env, timeout=300)
+        return float(r.stdout.decode().strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        return None
+
+
 def cpu_baseline(b: workloads.Batch, budget_s: float = 15.0):
     seqs, sb, dt = cpu_sample_plan(b, budget_s / 2)
     t0 = time.perf_counter()
     oracle_step(sb)
     dt = time.perf_counter() - t0
     toks = int(sb.cu_seqlens_q[-1])
+    dt1 = oracle_seconds_one_thread(sb)
     return {"value": toks / dt, "unit": "query tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "threads": "numpy's default BLAS / OpenMP pools (one per core)",
+            "one_thread": None if dt1 is None else {"value": toks / dt1, "cores": 1,
+                                                    "seconds": dt1},
             "sample": f"{len(seqs)} of {b.num_seqs} sequences of the same batch ({toks} query tokens; "
                       f"chunks cut to their first 128 queries at their own prior context; only "
                       f"their referenced blocks), append + attention in float64 numpy, {dt:.2f} s"}
