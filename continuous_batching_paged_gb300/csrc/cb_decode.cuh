@@ -1,11 +1,13 @@
 // Decode pass of ragged paged attention: every sequence with q_len == 1 attends to all of its
-// kv_len keys.  "Decode still reads the full KV every step" ("LLM learning path 3.3 Batching &
-// Memory Management", section "Common pitfalls"), so this pass is bound by HBM bandwidth and
-// is built around moving K/V pages at full rate:
+// kv_len keys.  Each decode step streams a sequence's whole cached K/V once for one query token
+// (the point "LLM learning path 3.3 Batching & Memory Management" makes in its section "Common
+// pitfalls"), so this pass is bound by HBM bandwidth and is built around moving K/V pages at
+// full rate:
 //
 //   * The key tiles of all decode sequences are laid end to end (16 keys per tile) and cut into
-//     `decode_ctas` equal contiguous ranges, one per CTA: every CTA streams the same number of
-//     bytes whatever the length mix.  A sequence cut by range boundaries leaves per-CTA partial
+//     N equal contiguous ranges (N from the planner, at most `decode_ctas`), one per working
+//     CTA: every CTA streams the same number of bytes whatever the length mix.  The CTAs are
+//     the first CTAs of the attention kernel (cb_attention.cu); the chunk pass's CTAs follow.  A sequence cut by range boundaries leaves per-CTA partial
 //     results (m, l, o) in the workspace; the last warp to finish a (sequence, KV head) merges
 //     them (an atomic counter per pair decides which): the split-KV scheme with an online
 //     softmax and a log-sum-exp merge, without a separate merge launch.

@@ -1,7 +1,7 @@
-// Chunk pass of ragged paged attention: sequences with q_len > 1 (chunked prefill).  "The
-// prefill chunks make the iteration compute-bound" ("LLM learning path 3.3 Batching & Memory
-// Management", section "Chunked prefill"), so this pass runs on the 5th-generation tensor
-// cores.  A chunk of queries attends to a cache that already holds the earlier chunks: query i
+// Chunk pass of ragged paged attention: sequences with q_len > 1 (chunked prefill).  A chunk's
+// many queries reuse each K/V tile, so this part of a step is limited by arithmetic rather than
+// by memory ("LLM learning path 3.3 Batching & Memory Management", section "Chunked prefill"),
+// and this pass runs on the 5th-generation tensor cores.  A chunk of queries attends to a cache that already holds the earlier chunks: query i
 // of a chunk with prior context ctx sees keys 0 .. ctx + i (same section).
 //
 // One work item = two 128-query tiles A and B that read the same K/V tiles: with an even GQA
