@@ -1,0 +1,55 @@
+"""Seeded random ragged batches through the CUDA path, element by element against the oracle:
+decode tokens, chunks of many lengths (ragged last tiles), empty sequences, GQA groups 1-8,
+head dims 64 and 128, block sizes 4-64, shuffled pages, sliding windows on some batches, and the
+one-call append + attention entry on others."""
+import numpy as np
+import pytest
+import torch
+
+import continuous_batching_paged_gb300 as cb
+import workloads
+from gpu_util import DeviceBatch, assert_close, bits_of, oracle_append
+from oracle import paged_attention as opa
+
+pytestmark = pytest.mark.gpu
+
+
+def _random_batch(trial):
+    rng = np.random.default_rng(9000 + trial)
+    S = int(rng.integers(1, 24))
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    D = int(rng.choice([64, 128]))
+    bs = int(rng.choice([4, 16, 32, 64]))
+    q_lens, kv_lens = [], []
+    for _ in range(S):
+        kind = rng.random()
+        q = 0 if kind < 0.1 else 1 if kind < 0.6 else int(rng.integers(2, 300))
+        ctx = int(rng.integers(0, 1500))
+        q_lens.append(q)
+        kv_lens.append(max(q + ctx, 1) if q == 0 else q + ctx)
+    b = workloads.build_batch(q_lens, kv_lens, G * Hkv, Hkv, D, bs, seed=9100 + trial,
+                              shuffle_pages=True, name=f"random {trial}")
+    window = int(rng.choice([0, 0, 0, 64, 300]))
+    return b, window
+
+
+@pytest.mark.parametrize("trial", range(10))
+def test_random_ragged_batch_matches_oracle(cuda_lib, trial):
+    b, window = _random_batch(trial)
+    db = DeviceBatch(b)
+    fused = trial % 2 == 1
+    if fused:
+        out = cb.append_attention(db.q, db.k_new, db.v_new, db.k_pages, db.v_pages,
+                                  db.block_table, db.cu, db.kv_lens, b.block_size, b.scale,
+                                  window=window)
+    else:
+        db.append()
+        out = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
+                                        db.kv_lens, b.block_size, b.scale, window=window)
+    assert cb.get_device_error() == cb.CB_OK
+    kp, vp = oracle_append(b)
+    assert np.array_equal(bits_of(db.k_pages), kp) and np.array_equal(bits_of(db.v_pages), vp)
+    ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                        b.block_size, b.scale, window=window)
+    assert_close(out.float().cpu().numpy(), ref, f"{b.name} (window {window}, fused {fused})")
