@@ -270,12 +270,35 @@ def sub_batch(b: workloads.Batch, seqs, chunk_rows=None) -> workloads.Batch:
                            num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
 
 
-def oracle_step(sb: workloads.Batch):
+def oracle_step(sb: workloads.Batch, window: int = 0):
+    """Append + attention of the sample in the oracle; returns its output rows [T, Hq, D]."""
     from oracle import paged_attention as opa
     kp, vp = opa.kv_append(sb.k_new, sb.v_new, sb.k_pages, sb.v_pages, sb.block_table,
                            sb.cu_seqlens_q, sb.kv_lens, sb.block_size)
-    opa.ragged_paged_attention(sb.q, kp, vp, sb.block_table, sb.cu_seqlens_q, sb.kv_lens,
-                               sb.block_size, sb.scale)
+    out, _ = opa.ragged_paged_attention(sb.q, kp, vp, sb.block_table, sb.cu_seqlens_q,
+                                        sb.kv_lens, sb.block_size, sb.scale, window=window)
+    return out
+
+
+def sample_rows(b: workloads.Batch, seqs, chunk_rows=128):
+    """Token indices of the full batch that sub_batch(b, seqs, chunk_rows) keeps, in its order."""
+    q_lens = np.diff(b.cu_seqlens_q)
+    rows = []
+    for s in seqs:
+        c0 = int(b.cu_seqlens_q[s])
+        rows.extend(range(c0, c0 + min(int(q_lens[s]), chunk_rows)))
+    return np.asarray(rows, dtype=np.int64)
+
+
+def parity_of(gpu_rows: np.ndarray, ref: np.ndarray):
+    """The bench's own parity line: the CUDA output rows of the oracle's sample against the
+    oracle, with the bar the parity tests use (|gpu - ref| <= 2e-2 + 1e-2 |ref|)."""
+    gpu = gpu_rows.astype(np.float64)
+    err = np.abs(gpu - ref)
+    return {"rows_checked": int(ref.shape[0]), "values_checked": int(ref.size),
+            "max_abs_err": float(err.max()), "max_rel_err": float((err / np.maximum(np.abs(ref), 1e-3)).max()),
+            "within_bar": bool(np.isfinite(gpu).all() and (err <= 2e-2 + 1e-2 * np.abs(ref)).all()),
+            "bar": "|gpu - ref| <= 2e-2 + 1e-2 |ref| elementwise"}
 
 
 def cpu_sample_plan(b: workloads.Batch, budget_s: float):
@@ -325,14 +348,18 @@ def oracle_seconds_one_thread(sb: workloads.Batch):
         return None
 
 
-def cpu_baseline(b: workloads.Batch, budget_s: float = 15.0):
+def cpu_baseline(b: workloads.Batch, budget_s: float = 15.0, gpu_out=None, window: int = 0):
     seqs, sb, dt = cpu_sample_plan(b, budget_s / 2)
     t0 = time.perf_counter()
-    oracle_step(sb)
+    ref = oracle_step(sb, window)
     dt = time.perf_counter() - t0
     toks = int(sb.cu_seqlens_q[-1])
     dt1 = oracle_seconds_one_thread(sb)
+    parity = None
+    if gpu_out is not None:  # the CUDA path's rows of the same sample, as float32 numpy
+        parity = parity_of(gpu_out(sample_rows(b, seqs)), ref)
     return {"value": toks / dt, "unit": "query tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "parity_vs_cuda": parity,
             "threads": "numpy's default BLAS / OpenMP pools (one per core)",
             "one_thread": None if dt1 is None else {"value": toks / dt1, "cores": 1,
                                                     "seconds": dt1},
@@ -890,7 +917,9 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(b)
+        cpu = cpu_baseline(
+            b, gpu_out=lambda rows: out[torch.from_numpy(rows).to(dev)].float().cpu().numpy(),
+            window=args.window)
 
     line = {
         "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
