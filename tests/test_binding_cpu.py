@@ -46,3 +46,14 @@ def test_block_moves_refuse_host_tensors():
     ids = torch.tensor([0, 1], dtype=torch.int32)
     with pytest.raises(ValueError):
         cb.copy_blocks(kp, vp, ids, ids.flip(0), 16)
+
+
+def test_graph_buckets_pad_sequences_and_tokens_to_their_intervals():
+    from continuous_batching_paged_gb300.graphs import GraphedStep
+    pool = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16)
+    g = GraphedStep(pool, pool, 16, 0.125, 4, 8, seq_interval=16, token_interval=64)
+    assert g.bucket_of(1, 1) == (16, 64)
+    assert g.bucket_of(16, 64) == (16, 64)
+    assert g.bucket_of(17, 65) == (32, 128)
+    assert g.bucket_of(121, 2048) == (128, 2048)
+    assert g.captures == 0 and len(g.cache) == 0      # nothing is captured without a device
