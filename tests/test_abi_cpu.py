@@ -98,5 +98,23 @@ def test_host_validation_rejects_before_cuda(lib):
     assert st == cb.CB_ERR_INVALID_ARG and b"null" in lib.cb_last_error_message()
 
 
+def test_new_entries_validate_on_the_host(lib):
+    # the one-call step and the pass time stamps reject bad arguments before any CUDA call
+    p = ctypes.c_void_p(256)
+    dims = _dims()
+    st = lib.cb_append_attention(None, p, p, p, p, p, p, p, 16, 0.125, p, None, p, 1 << 30,
+                                 ctypes.byref(dims), None, None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"null" in lib.cb_last_error_message()
+    st = lib.cb_append_attention(ctypes.c_void_p(264), p, p, p, p, p, p, p, 16, 0.125, p, None,
+                                 p, 1 << 30, ctypes.byref(dims), None, None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"16-byte" in lib.cb_last_error_message()
+    st = lib.cb_append_attention(p, p, p, p, p, p, p, p, 3, 0.125, p, None, p, 1 << 30,
+                                 ctypes.byref(dims), None, None)
+    assert st == cb.CB_ERR_INVALID_ARG and b"at least 4" in lib.cb_last_error_message()
+    ts = (ctypes.c_uint64 * 4)()
+    assert lib.cb_pass_timestamps(None, ts, None) == cb.CB_ERR_INVALID_ARG
+    assert lib.cb_pass_timestamps(p, None, None) == cb.CB_ERR_INVALID_ARG
+
+
 def test_build_flags_target_sm103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
