@@ -50,8 +50,7 @@ class DeviceBatch:
         # never written shows up as NaN in the output.
         ws = torch.full((cb.workspace_size(self.b.num_seqs, self.b.num_q_heads,
                                            self.b.num_kv_heads, self.b.head_dim,
-                                           self.b.num_pages, self.b.max_blocks,
-                                           self.b.block_size, self.b.num_tokens),), 255,
+                                           self.b.num_tokens),), 255,
                                            dtype=torch.uint8,
                         device="cuda")
         return cb.ragged_paged_attention(workspace=ws, *(
@@ -80,6 +79,8 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rtol=RT
     bad = err > atol + rtol * np.abs(ref)
     if bad.any():
         idx = np.argwhere(bad)[:5].tolist()
+        rel = float((err / np.maximum(np.abs(ref), 1e-6)).max())
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside "
-                             f"{atol} + {rtol}*|ref|; max abs err {err.max():.4g}; first {idx}")
-    return float(err.max())
+                             f"{atol} + {rtol}*|ref|; max abs err {err.max():.4g}, max rel err "
+                             f"{rel:.4g}; first {idx}")
+    return float(err.max()) if err.size else 0.0

@@ -197,47 +197,24 @@ def test_bad_block_id_reported_without_fault(cuda_lib):
 
 # ----------------------------------------------------------------------------- full-size configs
 
-def _sample_rows(b, rng, n_random=400):
-    q_lens = np.diff(b.cu_seqlens_q)
-    rows = set()
-    H = b.num_q_heads
-    for s in range(b.num_seqs):
-        c0 = int(b.cu_seqlens_q[s])
-        n = int(q_lens[s])
-        if n == 1:
-            rows.add((c0, int(rng.integers(H))))
-        elif n > 1:
-            for i in {0, 1, 127, 128, 129, n - 1, n - 2} & set(range(n)):
-                rows.add((c0 + i, int(rng.integers(H))))
-    T = b.num_tokens
-    for _ in range(n_random):
-        rows.add((int(rng.integers(T)), int(rng.integers(H))))
-    return sorted(rows)
-
-
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_configs_full_size(cuda_lib, cfg):
+    # every element of out and lse of the named full-size batches against the oracle: the
+    # decode-only and long-tail batches, the mixed 2048-token batch (a 1928-query chunk at prior
+    # context 3000 beside 120 decodes) and the chunk-heavy batch (8 chunks of 512 queries at
+    # prior contexts up to 8192, K x4), in the launch configuration the bench times
     b = named_config(cfg)
     db = DeviceBatch(b)
     db.append()
     out, lse = db.attend(lse=True)
     assert cb.get_device_error() == cb.CB_OK
     gpu = out.float().cpu().numpy()
-    assert np.isfinite(gpu).all()
     kp, vp = oracle_append(b)
-    if cfg in (2, 5):
-        ref, ref_lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
-                                                  b.kv_lens, b.block_size, b.scale)
-        assert_close(gpu, ref, b.name)
-        assert_close(lse.cpu().numpy(), ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
-    else:
-        rows = _sample_rows(b, np.random.default_rng(cfg))
-        ref, ref_lse = opa.attention_rows(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
-                                          b.block_size, b.scale, rows)
-        t_idx = [t for t, _ in rows]
-        h_idx = [h for _, h in rows]
-        assert_close(gpu[t_idx, h_idx], ref, b.name)
-        assert_close(lse.cpu().numpy()[t_idx, h_idx], ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
+    assert np.array_equal(bits_of(db.k_pages), kp) and np.array_equal(bits_of(db.v_pages), vp)
+    ref, ref_lse = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q,
+                                              b.kv_lens, b.block_size, b.scale)
+    assert_close(gpu, ref, b.name)
+    assert_close(lse.cpu().numpy(), ref_lse, b.name + " lse", atol=1e-3, rtol=1e-3)
 
 
 # ----------------------------------------------------------------------------- sliding window
@@ -321,8 +298,8 @@ def test_pass_timestamps_mark_the_passes_that_ran(cuda_lib, q_lens, kv_lens, has
                               max_blocks=160, shuffle_pages=True, name="stamps")
     db = DeviceBatch(b)
     db.append()
-    ws = torch.empty(cb.workspace_size(b.num_seqs, 8, 2, 128, b.num_pages, b.max_blocks, 16,
-                                       b.num_tokens), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(cb.workspace_size(b.num_seqs, 8, 2, 128, b.num_tokens), dtype=torch.uint8,
+                     device="cuda")
     out = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
                                     db.kv_lens, 16, b.scale, workspace=ws)
     ts = cb.pass_timestamps(ws)
