@@ -511,7 +511,7 @@ def run_serve(args, local: int):
     k_all = torch.randn((budget, Hkv, D), device=dev).to(torch.bfloat16)
     v_all = torch.randn((budget, Hkv, D), device=dev).to(torch.bfloat16)
     out = torch.empty_like(q_all)
-    ws = torch.empty(cb.workspace_size(cap, Hq, Hkv, D, P, MB, bs, budget), dtype=torch.uint8,
+    ws = torch.empty(cb.workspace_size(cap, Hq, Hkv, D, budget), dtype=torch.uint8,
                      device=dev)
     nbuf = 3  # pinned metadata ring: the host fills step k+1 while the GPU reads step k
     h_meta = [torch.empty(cap + 1 + cap + cap * MB + 2 * cap, dtype=torch.int32).pin_memory()
@@ -612,7 +612,7 @@ def run_graphs(args, local: int):
         tab, cu, kv = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
         out = torch.empty_like(q)
         ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
-                                           b.num_pages, b.max_blocks, b.block_size, b.num_tokens),
+                                           b.num_tokens),
                          dtype=torch.uint8, device=dev)
 
         def eager():
@@ -688,7 +688,7 @@ def main():
     table, cu, kvl = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
     out = torch.empty_like(q)
     ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
-                                       b.num_pages, b.max_blocks, b.block_size, b.num_tokens),
+                                       b.num_tokens),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

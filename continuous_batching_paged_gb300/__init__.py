@@ -77,7 +77,7 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.cb_last_error_message.restype = ctypes.c_char_p
     lib.cb_last_error_message.argtypes = []
     lib.cb_attention_workspace_size.restype = ctypes.c_size_t
-    lib.cb_attention_workspace_size.argtypes = [ctypes.POINTER(CbDims), ctypes.c_int32]
+    lib.cb_attention_workspace_size.argtypes = [ctypes.POINTER(CbDims)]
     lib.cb_kv_append.restype = ctypes.c_int
     lib.cb_kv_append.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int32,
                                  ctypes.POINTER(CbDims), _P]
@@ -257,10 +257,11 @@ def kv_append(k_new, v_new, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens
     _check(st, "cb_kv_append")
 
 
-def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_blocks,
-                   block_size, num_tokens) -> int:
-    dims = _dims(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_pages, max_blocks)
-    return int(library().cb_attention_workspace_size(ctypes.byref(dims), int(block_size)))
+def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_tokens) -> int:
+    """Bytes of device workspace an attention call on this batch shape needs
+    (cb_attention_workspace_size; 0 for an invalid shape)."""
+    dims = _dims(num_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, 1, 1)
+    return int(library().cb_attention_workspace_size(ctypes.byref(dims)))
 
 
 def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_lens, block_size,
@@ -298,7 +299,7 @@ def ragged_paged_attention(q, k_pages, v_pages, block_table, cu_seqlens_q, kv_le
         _require(lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == (T, Hq),
                  "lse must be a contiguous fp32 [T, Hq] tensor")
     dims = _dims(T, S, Hq, Hkv, D, P, block_table.shape[1])
-    need = int(library().cb_attention_workspace_size(ctypes.byref(dims), int(block_size)))
+    need = int(library().cb_attention_workspace_size(ctypes.byref(dims)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _require(workspace.dtype == torch.uint8 and workspace.is_contiguous(), "workspace must be uint8")

@@ -34,6 +34,7 @@ cb_status cuda_fail(cudaError_t e, const char* what) {
 
 struct DeviceState {
   bool ready = false;
+  unsigned long long ctx_id = 0;  // context the cached addresses belong to
   int sm_count = 0;
   uint32_t* err = nullptr;
 };
@@ -42,15 +43,55 @@ constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+std::once_flag g_driver_once;
+thread_local unsigned long long t_ctx_id = 0;
+
+// Driver entry points the library calls directly (it links the CUDA runtime only).
+void load_driver_entry_points() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+          cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+// Unique id of the calling thread's current CUDA context (0 when none is current yet).
+// Device addresses looked up in one context are meaningless in the next (after a
+// cudaDeviceReset, for instance), so every cached address is kept together with this id.
+cb_status context_id(unsigned long long* id) {
+  std::call_once(g_driver_once, load_driver_entry_points);
+  *id = 0;
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr)
+    return fail(CB_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId entry points unavailable");
+  CUcontext c = nullptr;
+  if (g_ctx_get_current(&c) != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (c != nullptr && g_ctx_get_id(c, id) != CUDA_SUCCESS)
+    return fail(CB_ERR_CUDA, "cuCtxGetId failed");
+  return CB_OK;
+}
 
 cb_status device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(CB_ERR_UNSUPPORTED, "device id %d", dev);
+  unsigned long long ctx = 0;
+  cb_status cst = context_id(&ctx);
+  if (cst != CB_OK) return cst;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& st = g_dev[dev];
-  if (!st.ready) {
+  if (!st.ready || ctx == 0 || st.ctx_id != ctx) {
+    st.ready = false;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -60,20 +101,16 @@ cb_status device_state(DeviceState** out) {
     e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_cb_error_word);
+    e = cudaGetSymbolAddress(&p, g_cb_error_word);  // also makes the device's context current
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     st.err = static_cast<uint32_t*>(p);
-    if (g_encode == nullptr) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    if (g_encode == nullptr)
+      return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    if ((cst = context_id(&ctx)) != CB_OK) return cst;
+    st.ctx_id = ctx;
     st.ready = true;
   }
+  t_ctx_id = st.ctx_id;
   *out = &st;
   return CB_OK;
 }
@@ -134,6 +171,11 @@ cb_status set_last_error(cb_status st, const char* msg) {
   t_last_error = msg;
   return st;
 }
+// Id of the calling thread's current context, for caches of device addresses and per-context
+// settings in other translation units (0 when no context is current).
+cb_status current_context_id(unsigned long long* id) { return context_id(id); }
+// The context of the last device_state() on this thread: the one the next launch goes to.
+unsigned long long launch_context_id() { return t_ctx_id; }
 }  // namespace cb
 
 extern "C" {
@@ -154,8 +196,12 @@ const char* cb_status_string(cb_status s) {
 
 const char* cb_last_error_message(void) { return t_last_error.c_str(); }
 
-size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size) {
-  if (check_dims(dims, block_size) != CB_OK) return 0;
+size_t cb_attention_workspace_size(const cb_dims* dims) {
+  // The size depends on the sequence, token and query-head counts and the head dim only.
+  if (dims == nullptr || dims->num_seqs < 0 || dims->num_tokens < 0 || dims->num_q_heads < 1 ||
+      dims->num_kv_heads < 1 || dims->num_q_heads % dims->num_kv_heads != 0 ||
+      (dims->head_dim != 64 && dims->head_dim != 128))
+    return 0;
   return cb::ws_layout(dims->num_seqs, dims->num_tokens, dims->num_q_heads, dims->head_dim).total;
 }
 

@@ -53,14 +53,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D, int NTH, bool kWin>
 static cudaError_t launch_instance(const AttnArgs& a, const AttnMaps& m, cudaStream_t stream) {
   constexpr int kSmem = AttnSmem<D>::kTotal;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  // The shared-memory opt-in is a setting of the context: made again whenever the launch
+  // goes to another context than the last one configured.
+  static unsigned long long configured_ctx = 0;
+  const unsigned long long ctx = launch_context_id();
+  if (ctx == 0 || configured_ctx != ctx) {
     const cudaError_t e = cudaFuncSetAttribute(
         attention_kernel<D, NTH, kWin>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_ctx = ctx;
   }
   // Programmatic stream serialization: the kernel may launch before the preceding launch on
   // the stream (the planner) ends, and waits for it with griddepcontrol.wait, so its launch

@@ -53,6 +53,10 @@ struct BlockMoveArgs {
   uint32_t* err;
 };
 
+// Id of the CUDA context the calling thread's next launch goes to (set by every API entry
+// point before it launches; 0 if unknown).
+unsigned long long launch_context_id();
+
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_block_move(const BlockMoveArgs& a, int sm_count, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, uint64_t* waited_ns,

@@ -37,8 +37,7 @@ class _Bucket:
         self.cu = torch.zeros(S + 1, dtype=torch.int32, device=dev)
         self.kv = torch.zeros(S, dtype=torch.int32, device=dev)
         self.table = torch.full((S, o.MB), -1, dtype=torch.int32, device=dev)
-        P = o.k_pages.shape[0]
-        self.ws = torch.empty(workspace_size(S, o.Hq, o.Hkv, o.D, P, o.MB, o.bs, T),
+        self.ws = torch.empty(workspace_size(S, o.Hq, o.Hkv, o.D, T),
                               dtype=torch.uint8, device=dev)
 
         def body():

@@ -96,12 +96,14 @@ cb_status cb_kv_append(const void* k_new, const void* v_new, void* k_pages, void
 
 /*
  * cb_attention_workspace_size -- bytes of device scratch cb_ragged_paged_attention needs.
- * Pure host arithmetic on (dims, block_size); 0 when dims is NULL or invalid.  The
- * workspace holds the batch plan (including the longest-first order of the chunk work, one
- * int32 per 128 query tokens plus one per sequence) and the fp32 partial results of split
- * decode sequences; it grows with num_seqs, num_tokens, num_q_heads and head_dim.
+ * Pure host arithmetic on num_seqs, num_tokens, num_q_heads, num_kv_heads and head_dim (the
+ * other fields of dims do not change the size and are not checked here); 0 when dims is NULL
+ * or those fields are invalid.  The workspace holds the batch plan (including the
+ * longest-first order of the chunk work, one int32 per 128 query tokens plus one per
+ * sequence) and the fp32 partial results of split decode sequences; it grows with num_seqs,
+ * num_tokens, num_q_heads and head_dim.
  */
-size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size);
+size_t cb_attention_workspace_size(const cb_dims* dims);
 
 /*
  * cb_ragged_paged_attention -- one attention forward pass over the ragged batch.
@@ -109,10 +111,19 @@ size_t cb_attention_workspace_size(const cb_dims* dims, int32_t block_size);
  * out[t, h, :] = sum_j softmax_j(scale * q[t,h,:] . K_s[j,g,:]) * V_s[j,g,:] over the keys
  * j <= ctx_s + i of t's own sequence s, with K_s/V_s gathered through block_table and
  * g = h / (Hq/Hkv).  Inputs are bf16, accumulation is fp32, out is rounded to bf16.
+ * Sources: the packed token axis whose tokens attend only within their own sequence is
+ * "LLM learning path 3.3", section "Continuous (iteration-level) batching", and the "first
+ * principles" summary (attention masks that keep the packed sequences apart); the keys of a
+ * sequence are read through its block table ("LLM learning path 3.3", section "PagedAttention:
+ * block tables"; architecture doc, section "Memory management"); a chunk's query i sees the
+ * prior context plus the chunk's queries up to i ("LLM learning path 3.3", section "Chunked
+ * prefill"); decode tokens read the whole cached context every step (same page, section
+ * "Common pitfalls / misconceptions").  The query-head to KV-head mapping h / (Hq/Hkv) is not
+ * stated on the pages; it is the contiguous grouping of grouped-query attention.
  * If lse is not NULL it receives the natural log of each row's softmax normaliser.
  * Sequences with q_len == 0 are skipped; the pass reads the pages after cb_kv_append wrote
  * them (kv_lens include the appended tokens).  out must not alias q or the pages.
- * workspace: device memory of at least cb_attention_workspace_size(dims, block_size) bytes,
+ * workspace: device memory of at least cb_attention_workspace_size(dims) bytes,
  * 256-byte aligned, owned by the caller and not used by other work while this call runs.
  * Device errors as for cb_kv_append, plus CB_ERR_TIMEOUT if a bounded wait expired.
  */
@@ -204,12 +215,16 @@ cb_status cb_pass_timestamps(const void* workspace, uint64_t* ts_ns, void* strea
  * from one fixed device array of CB_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
  * that loads the library holds until the process exits.  The call allocates nothing.
  *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current) and keeps it with the id of the device's current context; a call made in a
+ *     later context of the device (after cudaDeviceReset, say) looks it up again.  Make the
+ *     first call on a device before any stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (other streams, or host
  *     threads without ordering between them) race on it.  Each call rewrites every scratch
  *     byte it later reads, so contents left by the previous call do no harm.
- *   - A batch whose scratch need, cb_attention_workspace_size(dims, block_size), exceeds
+ *   - A batch whose scratch need, cb_attention_workspace_size(dims), exceeds
  *     CB_NOALLOC_SCRATCH_BYTES is rejected with CB_ERR_UNSUPPORTED before anything is queued.
+ *   - cb_pass_timestamps is not available for these calls: it reads its time stamps from the
+ *     caller's workspace, and this entry point has none.
  * Arguments, results and errors are otherwise those of cb_ragged_paged_attention.
  */
 #define CB_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -57,16 +57,19 @@ def _dims(**kw):
 
 
 def test_workspace_size_is_host_arithmetic(lib):
-    n = lib.cb_attention_workspace_size(ctypes.byref(_dims()), 16)
+    n = lib.cb_attention_workspace_size(ctypes.byref(_dims()))
     assert n > 0 and n % 256 == 0
     # grows with the number of sequences, heads and tokens (the chunk-unit order), never with
-    # pages
-    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_seqs=400)), 16) > n
-    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_pages=999)), 16) == n
-    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_tokens=999999)), 16) > n
-    assert lib.cb_attention_workspace_size(ctypes.byref(_dims()), 3) == 0       # block_size < 4
-    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(head_dim=96)), 16) == 0
-    assert lib.cb_attention_workspace_size(None, 16) == 0
+    # the pool or the table width
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_seqs=400))) > n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_q_heads=8))) > n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_pages=999))) == n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(max_blocks_per_seq=999))) == n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_tokens=999999))) > n
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(head_dim=96))) == 0
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_q_heads=3))) == 0  # 3 % 2
+    assert lib.cb_attention_workspace_size(ctypes.byref(_dims(num_seqs=-1))) == 0
+    assert lib.cb_attention_workspace_size(None) == 0
 
 
 def _append_status(lib, dims, block_size, ptr=16):
