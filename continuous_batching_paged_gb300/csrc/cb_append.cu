@@ -56,7 +56,7 @@ __device__ __forceinline__ void append_tokens(const AppendArgs& a, int first_war
     const int c0 = __ldg(a.cu_seqlens_q + s), c1 = __ldg(a.cu_seqlens_q + s + 1);
     const int q_len = c1 - c0;
     const int kv = __ldg(a.kv_lens + s);
-    if (t < c0 || t >= c1 || kv < q_len) {
+    if (t < c0 || t >= c1 || c1 > a.T || kv < q_len) {
       if (lane == 0) report(a.err, kErrOutOfRange);
       continue;
     }
@@ -98,7 +98,19 @@ __device__ __forceinline__ void append_tokens(const AppendArgs& a, int first_war
   }
 }
 
+// Checks of cu_seqlens_q that no token's own search sees (cu[0] = 0, non-decreasing,
+// cu[S] <= T), spread over the grid's threads: a token of a malformed range may land in a
+// neighbouring sequence's range, so the stand-alone append reports the metadata itself.  (The
+// append + planner launch leaves this to the planner, which makes the same checks.)
+__device__ __forceinline__ void check_cu_seqlens(const AppendArgs& a) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.S; i += gridDim.x * blockDim.x) {
+    const int c0 = __ldg(a.cu_seqlens_q + i), c1 = __ldg(a.cu_seqlens_q + i + 1);
+    if (c1 < c0 || (i == 0 && c0 != 0) || (i == a.S - 1 && c1 > a.T)) report(a.err, kErrOutOfRange);
+  }
+}
+
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendArgs a) {
+  check_cu_seqlens(a);
   append_tokens<kAppendMaxChunks>(a, blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5),
                                   gridDim.x * (kAppendThreads / 32));
 }
