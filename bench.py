@@ -59,6 +59,8 @@ def parse_args():
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="mixed")
     p.add_argument("--decode-ctas", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", action="store_true",
+                   help="measure the headline workload only (skip the further batches)")
     p.add_argument("--serial", action="store_true",
                    help="run the decode pass and the chunk pass as two launches, one after the other")
     p.add_argument("--mode", choices=["path", "blocks", "serve", "graphs"], default="path",
@@ -171,7 +173,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is not None:
@@ -182,9 +184,15 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock and the throttle reasons seen, over the samples taken between host
+        times t0 and t1 (all samples when not given; the whole run if that window caught none,
+        which a window shorter than the 100 ms sampling period can)."""
+        lines = [l for t, l in self.lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        if not lines and t0 is not None:
+            lines = [l for t, l in self.lines if t >= t0 - 0.15] or [l for _, l in self.lines]
         rows = []
-        for line in self.lines:
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) != 8:
                 continue
@@ -237,37 +245,102 @@ def barrier(world):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def sub_batch(b: workloads.Batch, seqs, chunk_rows=None) -> workloads.Batch:
-    """The listed sequences of b as a batch of their own (a chunk keeps its prior context and
-    its first chunk_rows queries)."""
-    q_lens = np.diff(b.cu_seqlens_q)
-    new_q, new_kv, rows_q, rows_kv = [], [], [], []
+class BenchBatch:
+    """A named batch for the bench: the seeded layout (lengths, block tables) of
+    workloads.make_layout, with its values drawn N(0, 1) in bf16 by torch's generator on
+    `device` (K scaled by the layout's k_scale); pages outside the batch's tables hold values
+    too.  The oracle's sample copies the values it needs back from the device."""
+
+    def __init__(self, lay: workloads.Layout, seed: int, device):
+        import torch
+        self.lay = lay
+        self.device = device
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        T, Hq, Hkv, D = lay.num_tokens, lay.num_q_heads, lay.num_kv_heads, lay.head_dim
+
+        def draw(shape, scale=1.0):
+            x = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+            return x.mul_(scale) if scale != 1.0 else x   # 4 = 2^2: exact in bf16
+
+        self.k_pages = draw((lay.num_pages, lay.block_size, Hkv, D), lay.k_scale)
+        self.v_pages = draw((lay.num_pages, lay.block_size, Hkv, D))
+        self.q = draw((T, Hq, D))
+        self.k_new = draw((T, Hkv, D), lay.k_scale)
+        self.v_new = draw((T, Hkv, D))
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+        self.table, self.cu, self.kv = i32(lay.block_table), i32(lay.cu_seqlens_q), i32(lay.kv_lens)
+        self.q_h, self.k_new_h, self.v_new_h = (_bits(x) for x in (self.q, self.k_new, self.v_new))
+
+    def pages(self, ids: np.ndarray):
+        """bf16 bits of blocks `ids` of both pools, copied from the device."""
+        import torch
+        idx = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int64)).to(self.device)
+        return _bits(self.k_pages.index_select(0, idx)), _bits(self.v_pages.index_select(0, idx))
+
+
+class HostBenchBatch:
+    """The reference arm's batch: the same seeded layout as BenchBatch, with values drawn on
+    the host on demand (each block from its own seeded generator), so that the oracle's sample
+    costs only the blocks it reads."""
+
+    def __init__(self, lay: workloads.Layout, seed: int):
+        self.lay = lay
+        self.seed = seed
+        rng = np.random.default_rng([seed, 1])
+        T, Hq, Hkv, D = lay.num_tokens, lay.num_q_heads, lay.num_kv_heads, lay.head_dim
+        self.q_h = workloads.f32_to_bf16_bits(rng.standard_normal((T, Hq, D), dtype=np.float32))
+        self.k_new_h = workloads.f32_to_bf16_bits(
+            lay.k_scale * rng.standard_normal((T, Hkv, D), dtype=np.float32))
+        self.v_new_h = workloads.f32_to_bf16_bits(rng.standard_normal((T, Hkv, D), dtype=np.float32))
+
+    def pages(self, ids: np.ndarray):
+        lay = self.lay
+        shape = (lay.block_size, lay.num_kv_heads, lay.head_dim)
+        k = np.empty((len(ids),) + shape, dtype=np.uint16)
+        v = np.empty_like(k)
+        for i, blk in enumerate(ids):
+            rng = np.random.default_rng([self.seed, 2, int(blk)])
+            k[i] = workloads.f32_to_bf16_bits(lay.k_scale * rng.standard_normal(shape, dtype=np.float32))
+            v[i] = workloads.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+        return k, v
+
+
+def _bits(t) -> np.ndarray:
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def sub_batch(bb, seqs, chunk_rows=None) -> workloads.Batch:
+    """The listed sequences of the bench batch as a host batch of their own (a chunk keeps its
+    prior context and its first chunk_rows queries; only the blocks they reference)."""
+    lay = bb.lay
+    q_lens = lay.q_lens
+    new_q, new_kv, rows = [], [], []
     for s in seqs:
         n = int(q_lens[s])
-        ctx = int(b.kv_lens[s]) - n
+        ctx = int(lay.kv_lens[s]) - n
         if chunk_rows is not None and n > chunk_rows:
             n = chunk_rows
-        c0 = int(b.cu_seqlens_q[s])
-        rows_q.append(b.q[c0:c0 + n])
-        rows_kv.append((b.k_new[c0:c0 + n], b.v_new[c0:c0 + n]))
+        c0 = int(lay.cu_seqlens_q[s])
+        rows.append(np.arange(c0, c0 + n))
         new_q.append(n)
         new_kv.append(ctx + n)
+    rows = np.concatenate(rows)
     cu = np.zeros(len(seqs) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(new_q)
-    # Carry only the blocks the sampled sequences reference (same contents, renumbered).
-    table = b.block_table[list(seqs)].copy()
+    table = lay.block_table[list(seqs)].copy()
     used = np.unique(table[table >= 0])
-    remap = np.full(b.num_pages, -1, dtype=np.int32)
+    remap = np.full(lay.num_pages, -1, dtype=np.int32)
     remap[used] = np.arange(used.size, dtype=np.int32)
     table = np.where(table >= 0, remap[np.maximum(table, 0)], -1).astype(np.int32)
-    return workloads.Batch(name=b.name + "-sample", q=np.concatenate(rows_q),
-                           k_new=np.concatenate([k for k, _ in rows_kv]),
-                           v_new=np.concatenate([v for _, v in rows_kv]),
-                           k_pages=b.k_pages[used], v_pages=b.v_pages[used],
-                           block_table=table, cu_seqlens_q=cu,
-                           kv_lens=np.asarray(new_kv, dtype=np.int32), block_size=b.block_size,
-                           scale=b.scale, num_q_heads=b.num_q_heads,
-                           num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
+    kp, vp = bb.pages(used)
+    return workloads.Batch(name=lay.name + "-sample", q=bb.q_h[rows], k_new=bb.k_new_h[rows],
+                           v_new=bb.v_new_h[rows], k_pages=kp, v_pages=vp, block_table=table,
+                           cu_seqlens_q=cu, kv_lens=np.asarray(new_kv, dtype=np.int32),
+                           block_size=lay.block_size, scale=lay.scale,
+                           num_q_heads=lay.num_q_heads, num_kv_heads=lay.num_kv_heads,
+                           head_dim=lay.head_dim)
 
 
 def oracle_step(sb: workloads.Batch, window: int = 0):
@@ -280,12 +353,12 @@ def oracle_step(sb: workloads.Batch, window: int = 0):
     return out
 
 
-def sample_rows(b: workloads.Batch, seqs, chunk_rows=128):
-    """Token indices of the full batch that sub_batch(b, seqs, chunk_rows) keeps, in its order."""
-    q_lens = np.diff(b.cu_seqlens_q)
+def sample_rows(lay, seqs, chunk_rows=128):
+    """Token indices of the full batch that sub_batch(.., seqs, chunk_rows) keeps, in order."""
+    q_lens = lay.q_lens
     rows = []
     for s in seqs:
-        c0 = int(b.cu_seqlens_q[s])
+        c0 = int(lay.cu_seqlens_q[s])
         rows.extend(range(c0, c0 + min(int(q_lens[s]), chunk_rows)))
     return np.asarray(rows, dtype=np.int64)
 
@@ -301,10 +374,10 @@ def parity_of(gpu_rows: np.ndarray, ref: np.ndarray):
             "bar": "|gpu - ref| <= 2e-2 + 1e-2 |ref| elementwise"}
 
 
-def cpu_sample_plan(b: workloads.Batch, budget_s: float):
+def cpu_sample_plan(bb, budget_s: float, window: int = 0):
     """A bounded sample: decode sequences and (for chunks) the first 128 queries of each chunk,
     grown until one oracle pass takes about budget_s."""
-    q_lens = np.diff(b.cu_seqlens_q)
+    q_lens = bb.lay.q_lens
     dec = [int(s) for s in np.nonzero(q_lens == 1)[0]]
     chunks = [int(s) for s in np.nonzero(q_lens > 1)[0]]
     order = []
@@ -315,9 +388,9 @@ def cpu_sample_plan(b: workloads.Batch, budget_s: float):
             order.append(dec[i])
     n = 1
     while True:
-        sb = sub_batch(b, order[:n], chunk_rows=128)
+        sb = sub_batch(bb, order[:n], chunk_rows=128)
         t0 = time.perf_counter()
-        oracle_step(sb)
+        oracle_step(sb, window)
         dt = time.perf_counter() - t0
         if dt >= budget_s or n >= len(order):
             return order[:n], sb, dt
@@ -329,56 +402,59 @@ import pickle, sys, time
 sys.path.insert(0, sys.argv[1])
 import bench
 from oracle import paged_attention  # noqa: F401  (imported before the clock starts)
-sb = pickle.load(sys.stdin.buffer)
+sb, window = pickle.load(sys.stdin.buffer)
 t0 = time.perf_counter()
-bench.oracle_step(sb)
+bench.oracle_step(sb, window)
 print(time.perf_counter() - t0)
 """
 
 
-def oracle_seconds_one_thread(sb: workloads.Batch):
+def oracle_seconds_one_thread(sb: workloads.Batch, window: int = 0):
     """The same oracle pass in a child process whose BLAS / OpenMP pools have one thread."""
     import pickle
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     try:
-        r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT], input=pickle.dumps(sb),
+        r = subprocess.run([sys.executable, "-c", _ONE_THREAD, ROOT], input=pickle.dumps((sb, window)),
                            capture_output=True, env=env, timeout=300)
         return float(r.stdout.decode().strip().splitlines()[-1]) if r.returncode == 0 else None
     except (OSError, ValueError, IndexError, subprocess.SubprocessError):
         return None
 
 
-def cpu_baseline(b: workloads.Batch, budget_s: float = 15.0, gpu_out=None, window: int = 0):
-    seqs, sb, dt = cpu_sample_plan(b, budget_s / 2)
+def cpu_baseline(bb: BenchBatch, budget_s: float = 15.0, gpu_out=None, window: int = 0,
+                 one_thread: bool = True):
+    seqs, sb, _ = cpu_sample_plan(bb, budget_s / 2, window)
     t0 = time.perf_counter()
     ref = oracle_step(sb, window)
     dt = time.perf_counter() - t0
     toks = int(sb.cu_seqlens_q[-1])
-    dt1 = oracle_seconds_one_thread(sb)
+    dt1 = oracle_seconds_one_thread(sb, window) if one_thread else None
     parity = None
     if gpu_out is not None:  # the CUDA path's rows of the same sample, as float32 numpy
-        parity = parity_of(gpu_out(sample_rows(b, seqs)), ref)
+        parity = parity_of(gpu_out(sample_rows(bb.lay, seqs)), ref)
     return {"value": toks / dt, "unit": "query tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "parity_vs_cuda": parity,
+            "seconds": dt, "parity_vs_cuda": parity,
             "threads": "numpy's default BLAS / OpenMP pools (one per core)",
             "one_thread": None if dt1 is None else {"value": toks / dt1, "cores": 1,
                                                     "seconds": dt1},
-            "sample": f"{len(seqs)} of {b.num_seqs} sequences of the same batch ({toks} query tokens; "
-                      f"chunks cut to their first 128 queries at their own prior context; only "
-                      f"their referenced blocks), append + attention in float64 numpy, {dt:.2f} s"}
+            "sample": f"{len(seqs)} of {bb.lay.num_seqs} sequences of the same batch ({toks} query "
+                      f"tokens; chunks cut to their first 128 queries at their own prior context; "
+                      f"only their referenced blocks), append + attention in float64 numpy, "
+                      f"{dt:.2f} s"}
 
 
-def run_reference(args, b: workloads.Batch, rank: int, world: int):
+def run_reference(args, lay: workloads.Layout, seed: int, rank: int, world: int):
     if rank != 0:
         return
+    bb = HostBenchBatch(lay, seed)
     total = args.steps + args.warmup
     per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
-    seqs, sb, _ = cpu_sample_plan(b, per_step)
+    seqs, sb, _ = cpu_sample_plan(bb, per_step, args.window)
     for _ in range(args.warmup):
-        oracle_step(sb)
+        oracle_step(sb, args.window)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(sb)
+        oracle_step(sb, args.window)
     dt = time.perf_counter() - t0
     toks = int(sb.cu_seqlens_q[-1])
     value = toks * args.steps / dt
@@ -387,22 +463,28 @@ def run_reference(args, b: workloads.Batch, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(b, args),
+        "data": "synthetic", "config": workload_config(lay, args.workload, args),
         "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": value, "unit": unit,
-                         "sample": f"each step: {len(seqs)} of {b.num_seqs} sequences "
+                         "sample": f"each step: {len(seqs)} of {lay.num_seqs} sequences "
                                    f"({toks} query tokens; chunks cut to 128 queries)"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def workload_config(b: workloads.Batch, args):
-    return {"workload": workloads.CONFIGS[WORKLOADS[args.workload]], "seqs": b.num_seqs,
-            "query_tokens": b.num_tokens, "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
-            "head_dim": b.head_dim, "block_size": b.block_size, "pages": b.num_pages,
-            "seed": 1000 + WORKLOADS[args.workload],
+def workload_config(lay: workloads.Layout, name: str, args, overrides=None):
+    cfg = WORKLOADS[name] if name in WORKLOADS else None
+    desc = workloads.CONFIGS[cfg] if cfg is not None else name
+    if overrides:
+        desc += " -- with " + ", ".join(f"{k}={v}" for k, v in overrides.items())
+    return {"workload": desc, "seqs": lay.num_seqs,
+            "query_tokens": lay.num_tokens, "q_heads": lay.num_q_heads,
+            "kv_heads": lay.num_kv_heads, "head_dim": lay.head_dim, "block_size": lay.block_size,
+            "pages": lay.num_pages,
             "l2": "flushed before every timed step (512 MiB write, then 512 MiB read); KV also exceeds L2",
             "parallelism": f"replicas x{args.gpus}",
+            "values": "N(0,1) bf16 from torch's seeded device generator; lengths and block "
+                      "tables from the seeded layout",
             **({"window": args.window} if getattr(args, "window", 0) else {})}
 
 
@@ -655,41 +737,31 @@ def run_graphs(args, local: int):
                               "that writes them there (GraphedStep.buffers)"}), flush=True)
 
 
-def main():
-    args = parse_args()
-    if args.mode != "path":
-        world, rank, local = dist_setup(args)
-        if rank == 0:
-            {"blocks": run_blocks, "serve": run_serve, "graphs": run_graphs}[args.mode](args, local)
-        return
-    world, rank, local = dist_setup(args)
-    cfg = WORKLOADS[args.workload]
-    b = workloads.make_config(cfg, seed=1000 + cfg + 7919 * rank)
-    if args.impl == "reference":
-        run_reference(args, b, rank, world)
-        return
+# Further batches measured in the same run, after the headline batch: the other named
+# workloads, then shapes around the decode-only batch (its lengths with another GQA group
+# size, head dim or block size).  (key, named workload, shape overrides, oracle budget in
+# seconds, one-thread oracle figure too)
+SUB_WORKLOADS = [
+    ("decode", 2, {}, 3.0, True),
+    ("prefill", 4, {}, 3.0, False),
+    ("longtail", 5, {}, 3.0, False),
+    ("tiny", 1, {}, 1.0, True),
+    ("decode_gqa16", 2, {"num_q_heads": 128}, 1.0, False),
+    ("decode_d64", 2, {"head_dim": 64}, 1.0, False),
+    ("decode_bs16", 2, {"block_size": 16, "num_pages": 32768}, 1.0, False),
+    ("decode_bs4", 2, {"block_size": 4, "num_pages": 131072}, 1.0, False),
+]
 
-    import torch
-    import continuous_batching_paged_gb300 as cb
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (the CUDA path has no CPU fallback)")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    cb.library()
 
-    def t16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    def t32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
-
-    q, kn, vn = t16(b.q), t16(b.k_new), t16(b.v_new)
-    kp, vp = t16(b.k_pages), t16(b.v_pages)
-    table, cu, kvl = t32(b.block_table), t32(b.cu_seqlens_q), t32(b.kv_lens)
+def measure(args, cb, torch, dev, bb: BenchBatch, world: int, sampler, with_e2e: bool,
+            cpu_budget: float, one_thread: bool, rank: int, name: str, overrides=None):
+    """Time one batch's step (append + attention) and return its part of the JSON line."""
+    lay = bb.lay
+    q, kn, vn, kp, vp = bb.q, bb.k_new, bb.v_new, bb.k_pages, bb.v_pages
+    table, cu, kvl = bb.table, bb.cu, bb.kv
     out = torch.empty_like(q)
-    ws = torch.empty(cb.workspace_size(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
-                                       b.num_tokens),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(cb.workspace_size(lay.num_seqs, lay.num_q_heads, lay.num_kv_heads,
+                                       lay.head_dim, lay.num_tokens), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -699,10 +771,9 @@ def main():
         # lines whose write-back would be charged to the step's own DRAM traffic.
         flush.fill_(1.0)
         flush_r.sum()
-    stream = torch.cuda.current_stream()
 
     # ev_start / ev_end bracket the step on the launching stream; the library records its five
-    # phase events around the planner, the decode kernel and the chunk kernel (cb_options).
+    # phase events around the planner and the attention launch (cb_options).
     ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ph = [torch.cuda.Event(enable_timing=True) for _ in range(cb.NUM_PHASE_EVENTS)]
     for e in [ev_start, ev_end] + ph:
@@ -712,29 +783,18 @@ def main():
         kw = dict(out=out, workspace=ws, decode_ctas=args.decode_ctas,
                   phase_events=ph if record else None, serial=args.serial, window=args.window)
         if args.separate:
-            cb.kv_append(kn, vn, kp, vp, table, cu, kvl, b.block_size)
-            cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, b.block_size, b.scale, **kw)
+            cb.kv_append(kn, vn, kp, vp, table, cu, kvl, lay.block_size)
+            cb.ragged_paged_attention(q, kp, vp, table, cu, kvl, lay.block_size, lay.scale, **kw)
         else:
-            cb.append_attention(q, kn, vn, kp, vp, table, cu, kvl, b.block_size, b.scale, **kw)
+            cb.append_attention(q, kn, vn, kp, vp, table, cu, kvl, lay.block_size, lay.scale, **kw)
 
     # correctness guard before timing: the error word must be clear after one step
     step(False)
     cb.check_device_error()
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    t_start = time.perf_counter()
     for _ in range(args.warmup):
         flush_l2()
         step(False)
     torch.cuda.synchronize()
-    soak = 0
-    while time.perf_counter() - t_start < 2.0:   # let the clock sampler see the GPU under load
-        flush_l2()
-        step(False)
-        soak += 1
-        if soak % 50 == 0:
-            torch.cuda.synchronize()
 
     # Timed region: K steps, each bracketed by ev_start / ev_end on the launching stream; no
     # phase events inside (an event between two kernels costs the step a few microseconds).
@@ -753,12 +813,9 @@ def main():
         step_ms += per_step[-1]
     torch.cuda.synchronize()
     barrier(world)
-    wall = time.perf_counter() - wall0
-    sampler.stop()
+    wall1 = time.perf_counter()
     cb.check_device_error()
-
     ms = dist_max(step_ms / args.steps, world, dev)
-    value = world * b.num_tokens / (ms / 1000.0)
 
     # Kernel spans (roofline inputs): the same steps again with the library's phase events.
     # In the default (one attention launch) mode the decode and chunk passes share a launch:
@@ -792,17 +849,102 @@ def main():
     per_kernel = {n: dist_max(acc[n] / n_span, world, dev) for n in spans}
     role_ms = {n: dist_max(v / n_span, world, dev) for n, v in role.items()}
 
-    # e2e: the step through the public API with inputs from pinned host memory, output back.
-    h_q = torch.from_numpy(b.q.view(np.int16)).pin_memory()
-    h_k = torch.from_numpy(b.k_new.view(np.int16)).pin_memory()
-    h_v = torch.from_numpy(b.v_new.view(np.int16)).pin_memory()
-    h_tab = torch.from_numpy(b.block_table).pin_memory()
-    h_cu = torch.from_numpy(b.cu_seqlens_q).pin_memory()
-    h_kv = torch.from_numpy(b.kv_lens).pin_memory()
-    h_out = torch.empty(b.q.shape, dtype=torch.int16).pin_memory()
+    e2e = None
+    if with_e2e:
+        e2e = measure_e2e(args, cb, torch, dev, bb, ws, out, flush_l2, world)
+
+    pk, pk_kind = peaks()
+    dec_bytes, dec_logical = decode_kv_bytes(lay, args.window)
+    flops = chunk_flops(lay, args.window)
+    # Pass spans: with both passes in one launch, from the kernel's device time stamps; in
+    # serial mode (two launches), from the events around each launch.
+    dec_ms = per_kernel["decode"] if args.serial else role_ms["decode"]
+    chunk_ms = per_kernel["chunk"] if args.serial else role_ms["chunk"]
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 and dec_bytes else None
+    chunk_tf = flops / (chunk_ms * 1e-3) / 1e12 if chunk_ms > 0 and flops else None
+    # The roofline is taken on the attention kernel (one launch runs both passes; its span from
+    # the events around it), against the bound of the pass with the larger ideal time (work /
+    # peak).  In serial mode each pass is its own launch and is measured alone.
+    dec_ideal = dec_bytes / (pk["hbm_gbs"] * 1e9) if dec_bytes else 0.0
+    chunk_ideal = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
+    hbm_bound = dec_ideal >= chunk_ideal and dec_bytes > 0
+    if args.serial:
+        attn_ms = dec_ms if hbm_bound else chunk_ms
+    else:
+        attn_ms = per_kernel["attention"]
+    traffic = recorded_traffic("attention_kernel", name) if not overrides else None
+    if hbm_bound:
+        ach = dec_bytes / (attn_ms * 1e-3) / 1e9
+        roof = {"kernel": "attention_kernel", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": attn_ms,
+                "peak_kind": pk_kind, "frac_of_nominal_8000": ach / NOMINAL_HBM_GBS}
+    else:
+        tpk = pk["bf16_tflops"]
+        ach = flops / (attn_ms * 1e-3) / 1e12
+        roof = {"kernel": "attention_kernel", "bound": "tensor", "achieved": ach, "peak": tpk,
+                "unit": "TFLOP/s", "frac": ach / tpk, "traffic": traffic,
+                "algorithmic_flops_per_launch": flops, "launch_ms": attn_ms,
+                "peak_kind": pk_kind + " burst bf16"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(
+            bb, budget_s=cpu_budget, window=args.window, one_thread=one_thread,
+            gpu_out=lambda rows: out[torch.from_numpy(rows).to(dev)].float().cpu().numpy())
+
+    res = {
+        "value": world * lay.num_tokens / (ms / 1000.0), "unit": "query tokens/s",
+        "ms_per_step": ms,
+        "step_ms_stats": {"median": statistics.median(per_step), "min": min(per_step),
+                          "max": max(per_step)},
+        "config": workload_config(lay, name, args, overrides),
+        "roofline": roof,
+        "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
+                   "span_ms": dec_ms, "gbs": dec_gbs,
+                   "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,
+                   "frac_of_nominal_8000": (dec_gbs / NOMINAL_HBM_GBS) if dec_gbs else None},
+        "chunk": {"flops": flops, "span_ms": chunk_ms, "tflops": chunk_tf,
+                  "span_note": None if args.serial else
+                  "decode and chunk spans: first start to last end of each pass's CTAs with work "
+                  "(device %globaltimer stamps, cb_pass_timestamps); the chunk pass runs on the "
+                  "SMs the decode pass leaves free",
+                  "frac_of_burst": (chunk_tf / pk["bf16_tflops"]) if chunk_tf else None,
+                  "frac_of_sustained": (chunk_tf / pk["bf16_tflops_sustained"]) if chunk_tf else None},
+        "kernel_ms": per_kernel,
+        "clocks": sampler.summary(wall0, wall1),
+        "cpu_baseline": cpu,
+        "wall_s_timed": wall1 - wall0,
+    }
+    if e2e is not None:
+        res["e2e"] = e2e
+    return res
+
+
+def measure_e2e(args, cb, torch, dev, bb: BenchBatch, ws, out, flush_l2, world):
+    """The step through the public API with inputs from pinned host memory, output back."""
+    lay = bb.lay
+    q, kn, vn, kp, vp = bb.q, bb.k_new, bb.v_new, bb.k_pages, bb.v_pages
+    table, cu, kvl = bb.table, bb.cu, bb.kv
+    h_q = torch.from_numpy(bb.q_h.view(np.int16)).pin_memory()
+    h_k = torch.from_numpy(bb.k_new_h.view(np.int16)).pin_memory()
+    h_v = torch.from_numpy(bb.v_new_h.view(np.int16)).pin_memory()
+    h_tab = torch.from_numpy(lay.block_table).pin_memory()
+    h_cu = torch.from_numpy(lay.cu_seqlens_q).pin_memory()
+    h_kv = torch.from_numpy(lay.kv_lens).pin_memory()
+    h_out = torch.empty(tuple(q.shape), dtype=torch.int16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_cu, h_kv))
     d2h = h_out.numel() * h_out.element_size()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def run(bq, bk, bv, btab, bcu, bkv, bo):
+        kw = dict(out=bo, workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial,
+                  window=args.window)
+        if args.separate:
+            cb.kv_append(bk, bv, kp, vp, btab, bcu, bkv, lay.block_size)
+            cb.ragged_paged_attention(bq, kp, vp, btab, bcu, bkv, lay.block_size, lay.scale, **kw)
+        else:
+            cb.append_attention(bq, bk, bv, kp, vp, btab, bcu, bkv, lay.block_size, lay.scale, **kw)
 
     def e2e_step():
         q.view(torch.int16).copy_(h_q, non_blocking=True)
@@ -811,7 +953,7 @@ def main():
         table.copy_(h_tab, non_blocking=True)
         cu.copy_(h_cu, non_blocking=True)
         kvl.copy_(h_kv, non_blocking=True)
-        step(False)
+        run(q, kn, vn, table, cu, kvl, out)
         h_out.copy_(out.view(torch.int16), non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -857,13 +999,7 @@ def main():
             h2d_done[j].record(s_in)
         comp.wait_event(h2d_done[j])
         comp.wait_event(d2h_done[j])               # out buffer j has been read back
-        kw = dict(out=bo, workspace=ws, decode_ctas=args.decode_ctas, serial=args.serial,
-                  window=args.window)
-        if args.separate:
-            cb.kv_append(bk, bv, kp, vp, btab, bcu, bkv, b.block_size)
-            cb.ragged_paged_attention(bq, kp, vp, btab, bcu, bkv, b.block_size, b.scale, **kw)
-        else:
-            cb.append_attention(bq, bk, bv, kp, vp, btab, bcu, bkv, b.block_size, b.scale, **kw)
+        run(bq, bk, bv, btab, bcu, bkv, bo)
         comp_done[j].record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[j])
@@ -880,83 +1016,100 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = dist_max(1e3 * (time.perf_counter() - t0) / args.steps, world, dev)
     cb.check_device_error()
+    return {"value": world * lay.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "how": "wall clock over K steps; each step copies its inputs from pinned host "
+                   "memory and reads its output back, overlapped with the neighbouring "
+                   "steps' kernels (double buffers, copy streams)",
+            "serial_ms_per_step": e2e_serial_ms,
+            "serial_value": world * lay.num_tokens / (e2e_serial_ms / 1000.0)}
 
-    pk, pk_kind = peaks()
-    dec_bytes, dec_logical = decode_kv_bytes(b, args.window)
-    flops = chunk_flops(b, args.window)
-    # Pass spans: with both passes in one launch, from the kernel's device time stamps; in
-    # serial mode (two launches), from the events around each launch.
-    dec_ms = per_kernel["decode"] if args.serial else role_ms["decode"]
-    chunk_ms = per_kernel["chunk"] if args.serial else role_ms["chunk"]
-    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 and dec_bytes else None
-    chunk_tf = flops / (chunk_ms * 1e-3) / 1e12 if chunk_ms > 0 and flops else None
-    # The roofline is taken on the attention kernel (one launch runs both passes; its span from
-    # the events around it), against the bound of the pass with the larger ideal time (work /
-    # peak).  In serial mode each pass is its own launch and is measured alone.
-    dec_ideal = dec_bytes / (pk["hbm_gbs"] * 1e9) if dec_bytes else 0.0
-    chunk_ideal = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
-    hbm_bound = dec_ideal >= chunk_ideal and dec_bytes > 0
-    if args.serial:
-        attn_ms = dec_ms if hbm_bound else chunk_ms
-    else:
-        attn_ms = per_kernel["attention"]
-    traffic = recorded_traffic("attention_kernel", args.workload)
-    if hbm_bound:
-        ach = dec_bytes / (attn_ms * 1e-3) / 1e9
-        roof = {"kernel": "attention_kernel", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic,
-                "algorithmic_bytes_per_launch": dec_bytes, "launch_ms": attn_ms,
-                "peak_kind": pk_kind, "frac_of_nominal_8000": ach / NOMINAL_HBM_GBS}
-    else:
-        tpk = pk["bf16_tflops"]
-        ach = flops / (attn_ms * 1e-3) / 1e12
-        roof = {"kernel": "attention_kernel", "bound": "tensor", "achieved": ach, "peak": tpk,
-                "unit": "TFLOP/s", "frac": ach / tpk, "traffic": traffic,
-                "algorithmic_flops_per_launch": flops, "launch_ms": attn_ms,
-                "peak_kind": pk_kind + " burst bf16"}
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(
-            b, gpu_out=lambda rows: out[torch.from_numpy(rows).to(dev)].float().cpu().numpy(),
-            window=args.window)
+def main():
+    args = parse_args()
+    if args.mode != "path":
+        world, rank, local = dist_setup(args)
+        if rank == 0:
+            {"blocks": run_blocks, "serve": run_serve, "graphs": run_graphs}[args.mode](args, local)
+        return
+    world, rank, local = dist_setup(args)
+    cfg = WORKLOADS[args.workload]
+    seed = 1000 + cfg + 7919 * rank
+    lay = workloads.make_layout(cfg, seed=seed)
+    if args.impl == "reference":
+        run_reference(args, lay, seed, rank, world)
+        return
+
+    import torch
+    import continuous_batching_paged_gb300 as cb
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the CUDA path has no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cb.library()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    bb = BenchBatch(lay, seed, dev)
+    # Let the clock sampler see the GPU under load before the first timed region.
+    soak_ws = torch.empty(cb.workspace_size(lay.num_seqs, lay.num_q_heads, lay.num_kv_heads,
+                                            lay.head_dim, lay.num_tokens), dtype=torch.uint8,
+                          device=dev)
+    t_start = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t_start < 2.0:
+        cb.append_attention(bb.q, bb.k_new, bb.v_new, bb.k_pages, bb.v_pages, bb.table, bb.cu,
+                            bb.kv, lay.block_size, lay.scale, workspace=soak_ws,
+                            window=args.window)
+        n += 1
+        if n % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    del soak_ws
+
+    head = measure(args, cb, torch, dev, bb, world, sampler, with_e2e=True, cpu_budget=15.0,
+                   one_thread=True, rank=rank, name=args.workload)
+    del bb
+    torch.cuda.empty_cache()
+
+    subs = {}
+    if not args.only:
+        for key, n_cfg, over, budget, one_thr in SUB_WORKLOADS:
+            if key == args.workload:
+                continue
+            s_seed = 1000 + n_cfg + 7919 * rank
+            sub_lay = workloads.make_layout(n_cfg, seed=s_seed, **over)
+            sbb = BenchBatch(sub_lay, s_seed, dev)
+            base = [k for k, v in WORKLOADS.items() if v == n_cfg][0]
+            subs[key] = measure(args, cb, torch, dev, sbb, world, sampler, with_e2e=False,
+                                cpu_budget=budget, one_thread=one_thr, rank=rank, name=base,
+                                overrides=over or None)
+            del sbb
+            torch.cuda.empty_cache()
+    sampler.stop()
 
     line = {
-        "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "step_ms_stats": {"median": statistics.median(per_step), "min": min(per_step),
-                          "max": max(per_step)},
+        "metric": METRIC, "value": head["value"], "unit": "query tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "step_ms_stats": head["step_ms_stats"],
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(b, args),
-        "e2e": {"value": world * b.num_tokens / (e2e_ms / 1000.0), "unit": "query tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "how": "wall clock over K steps; each step copies its inputs from pinned host "
-                       "memory and reads its output back, overlapped with the neighbouring "
-                       "steps' kernels (double buffers, copy streams)",
-                "serial_ms_per_step": e2e_serial_ms,
-                "serial_value": world * b.num_tokens / (e2e_serial_ms / 1000.0)},
+        "config": head["config"],
+        "e2e": head["e2e"],
         # per step: append + plan (one launch) and attention (decode, merge, chunk in one
         # launch); --separate: append, plan, attention; --serial: one more (the passes apart)
         "gpu_launches": (2 + int(args.separate) + int(args.serial)) * args.steps,
         "append_attention": "two calls" if args.separate else "cb_append_attention",
         "concurrent_decode_chunk": not args.serial,
-        "roofline": roof,
-        "decode": {"kv_bytes_unique": dec_bytes, "kv_bytes_logical": dec_logical,
-                   "span_ms": dec_ms, "gbs": dec_gbs,
-                   "frac_of_measured": (dec_gbs / pk["hbm_gbs"]) if dec_gbs else None,
-                   "frac_of_nominal_8000": (dec_gbs / NOMINAL_HBM_GBS) if dec_gbs else None},
-        "chunk": {"flops": flops, "span_ms": chunk_ms, "tflops": chunk_tf,
-                  "span_note": None if args.serial else
-                  "decode and chunk spans: first start to last end of each pass's CTAs with work "
-                  "(device %globaltimer stamps, cb_pass_timestamps); the chunk pass runs on the "
-                  "SMs the decode pass leaves free",
-                  "frac_of_burst": (chunk_tf / pk["bf16_tflops"]) if chunk_tf else None,
-                  "frac_of_sustained": (chunk_tf / pk["bf16_tflops_sustained"]) if chunk_tf else None},
-        "kernel_ms": per_kernel,
-        "clocks": sampler.summary(),
-        "cpu_baseline": cpu,
-        "wall_s_timed": wall,
+        "roofline": head["roofline"],
+        "decode": head["decode"],
+        "chunk": head["chunk"],
+        "kernel_ms": head["kernel_ms"],
+        "clocks": head["clocks"],
+        "cpu_baseline": head["cpu_baseline"],
+        "wall_s_timed": head["wall_s_timed"],
+        "workloads": subs,
+        "clocks_whole_run": sampler.summary(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -111,34 +111,41 @@ def _draw(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
     return out
 
 
-def build_batch(
-    q_lens,
-    kv_lens,
-    num_q_heads: int,
-    num_kv_heads: int,
-    head_dim: int,
-    block_size: int,
-    seed: int,
-    *,
-    num_pages: int | None = None,
-    pool_factor: float = 1.25,
-    k_scale: float = 1.0,
-    shared_prefix: tuple[list[int], int] | None = None,
-    slack_blocks: int = 2,
-    max_blocks: int | None = None,
-    scale: float | None = None,
-    shuffle_pages: bool = True,
-    name: str = "custom",
-) -> Batch:
-    """Draw one ragged batch.
+@dataclasses.dataclass
+class Layout:
+    """The metadata of a batch without its values: lengths, block tables and shapes."""
+    name: str
+    block_table: np.ndarray
+    cu_seqlens_q: np.ndarray
+    kv_lens: np.ndarray
+    block_size: int
+    scale: float
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    num_pages: int
+    k_scale: float
 
-    q_lens[s] query tokens of sequence s are appended this step, so its prior
-    context is kv_lens[s] - q_lens[s] tokens, already in the cache.
-    ``shared_prefix=(members, n_tokens)`` makes the listed sequences point at the
-    same physical blocks for their first n_tokens (n_tokens must be a whole
-    number of blocks and every member must have at least that much prior context).
-    """
-    rng = np.random.default_rng(seed)
+    @property
+    def num_seqs(self) -> int:
+        return int(self.kv_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def q_lens(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q)
+
+
+def _layout(rng, q_lens, kv_lens, num_q_heads, num_kv_heads, head_dim, block_size, *,
+            num_pages=None, pool_factor=1.25, k_scale=1.0, shared_prefix=None, slack_blocks=2,
+            max_blocks=None, scale=None, shuffle_pages=True, name="custom"):
     q_lens = np.asarray(q_lens, dtype=np.int64)
     kv_lens = np.asarray(kv_lens, dtype=np.int64)
     S = len(q_lens)
@@ -180,10 +187,63 @@ def build_batch(
         table[s, start:start + cnt] = page_ids[nxt:nxt + cnt]
         nxt += cnt
 
-    H, Hkv, D = int(num_q_heads), int(num_kv_heads), int(head_dim)
-    T = int(q_lens.sum())
     cu = np.zeros(S + 1, dtype=np.int32)
     cu[1:] = np.cumsum(q_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(int(head_dim))
+    return Layout(name=name, block_table=table, cu_seqlens_q=cu,
+                  kv_lens=kv_lens.astype(np.int32), block_size=bs, scale=float(scale),
+                  num_q_heads=int(num_q_heads), num_kv_heads=int(num_kv_heads),
+                  head_dim=int(head_dim), num_pages=int(num_pages), k_scale=float(k_scale))
+
+
+def batch_layout(q_lens, kv_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 block_size: int, seed: int, **kw) -> Layout:
+    """The metadata build_batch would draw with the same arguments (the same block tables),
+    without drawing any values: for callers that fill the values elsewhere."""
+    return _layout(np.random.default_rng(seed), q_lens, kv_lens, num_q_heads, num_kv_heads,
+                   head_dim, block_size, **kw)
+
+
+def build_batch(
+    q_lens,
+    kv_lens,
+    num_q_heads: int,
+    num_kv_heads: int,
+    head_dim: int,
+    block_size: int,
+    seed: int,
+    *,
+    num_pages: int | None = None,
+    pool_factor: float = 1.25,
+    k_scale: float = 1.0,
+    shared_prefix: tuple[list[int], int] | None = None,
+    slack_blocks: int = 2,
+    max_blocks: int | None = None,
+    scale: float | None = None,
+    shuffle_pages: bool = True,
+    name: str = "custom",
+) -> Batch:
+    """Draw one ragged batch.
+
+    q_lens[s] query tokens of sequence s are appended this step, so its prior
+    context is kv_lens[s] - q_lens[s] tokens, already in the cache.
+    ``shared_prefix=(members, n_tokens)`` makes the listed sequences point at the
+    same physical blocks for their first n_tokens (n_tokens must be a whole
+    number of blocks and every member must have at least that much prior context).
+    """
+    rng = np.random.default_rng(seed)
+    lay = _layout(rng, q_lens, kv_lens, num_q_heads, num_kv_heads, head_dim, block_size,
+                  num_pages=num_pages, pool_factor=pool_factor, k_scale=k_scale,
+                  shared_prefix=shared_prefix, slack_blocks=slack_blocks, max_blocks=max_blocks,
+                  scale=scale, shuffle_pages=shuffle_pages, name=name)
+    table, cu, bs, num_pages = lay.block_table, lay.cu_seqlens_q, lay.block_size, lay.num_pages
+    kv_lens = lay.kv_lens.astype(np.int64)
+    q_lens = np.diff(cu).astype(np.int64)
+    S = lay.num_seqs
+    nblk = (kv_lens + bs - 1) // bs
+    H, Hkv, D = lay.num_q_heads, lay.num_kv_heads, lay.head_dim
+    T = int(q_lens.sum())
 
     # Referenced pages receive random content; everything else is poison.
     referenced = np.unique(table[table >= 0])
@@ -208,11 +268,9 @@ def build_batch(
     q = _draw(rng, (T, H, D))
     k_new = _draw(rng, (T, Hkv, D), k_scale)
     v_new = _draw(rng, (T, Hkv, D))
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     return Batch(name=name, q=q, k_new=k_new, v_new=v_new, k_pages=k_pages, v_pages=v_pages,
                  block_table=table, cu_seqlens_q=cu, kv_lens=kv_lens.astype(np.int32),
-                 block_size=bs, scale=float(scale), num_q_heads=H, num_kv_heads=Hkv, head_dim=D)
+                 block_size=bs, scale=lay.scale, num_q_heads=H, num_kv_heads=Hkv, head_dim=D)
 
 
 # Named workloads.  "ctx" is the prior context, so kv_len = ctx + q_len.
@@ -264,3 +322,13 @@ def make_config(n: int, seed: int | None = None) -> Batch:
         seed = 1000 + n
     q, kv, kw = config_lengths(n, seed)
     return build_batch(q, kv, seed=seed, name=f"config{n}", **kw)
+
+
+def make_layout(n: int, seed: int | None = None, **overrides) -> Layout:
+    """The metadata of named workload ``n`` (the block tables make_config draws with the same
+    seed), with optional shape overrides (head counts, head_dim, block_size)."""
+    if seed is None:
+        seed = 1000 + n
+    q, kv, kw = config_lengths(n, seed)
+    kw.update(overrides)
+    return batch_layout(q, kv, seed=seed, name=f"config{n}", **kw)
