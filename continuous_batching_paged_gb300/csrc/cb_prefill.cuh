@@ -217,11 +217,16 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         if (lane == 0) {
           if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
           mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kQTile);
-          for (int t = 0; t < (it.hasB ? 2 : 1); ++t)
+#pragma unroll
+          for (int half = 0; half < SM::kHalves; ++half)
+            tma_load_3d(sbase + SM::kQ0 + half * SM::kQHalf, qmap, bar(SM::bQFull), half * 64,
+                        it.head[0], it.tok[0]);
+          if (it.hasB) {
 #pragma unroll
             for (int half = 0; half < SM::kHalves; ++half)
-              tma_load_3d(sbase + SM::kQ0 + t * SM::kQTile + half * SM::kQHalf, qmap,
-                          bar(SM::bQFull), half * 64, it.head[t], it.tok[t]);
+              tma_load_3d(sbase + SM::kQ0 + SM::kQTile + half * SM::kQHalf, qmap, bar(SM::bQFull),
+                          half * 64, it.head[1], it.tok[1]);
+          }
         }
         const int32_t* row = a.block_table + (size_t)it.s * a.max_blocks;
         // Stage the item's block-table entries in shared memory with coalesced loads issued
@@ -289,7 +294,12 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
     } else if (warp == 1) {
       // =================================================================== tcgen05 issuer
       // The whole warp runs this loop (uniform control flow); one elected lane issues each
-      // batch of MMAs together with the commit that tracks it.
+      // batch of MMAs together with the commit that tracks it.  An MMA's issue returns only
+      // once the tensor core can queue it, about one MMA ahead of the one executing, so every
+      // instruction this thread runs between two batches is time the tensor core may sit idle:
+      // the loop keeps that work short (per-tile state in scalars, never in arrays indexed at
+      // run time, which would live in local memory; the tiles unrolled; descriptors
+      // precomputed).
       constexpr uint32_t idesc_s = idesc_bf16(kPrefillTileM, kChunkKeys, 0);
       constexpr uint32_t idesc_o = idesc_bf16(kPrefillTileM, D, 1);
       // Descriptor of the first 16-wide K slice of each operand region; a slice at byte offset
@@ -297,7 +307,9 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       const uint64_t q_desc0 = smem_desc_sw128(sbase + SM::kQ0, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sbase + SM::kStage0, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(sbase + SM::kStage0 + SM::kKVTile, SM::kKVHalf, 1024);
-      uint32_t g = 0, gx[2] = {0, 0}, kx[2] = {0, 0};
+      uint32_t g = 0;                // K/V tiles consumed so far (position in the stage ring)
+      uint32_t gxA = 0, gxB = 0;     // S/P rounds of tile A / tile B so far
+      uint32_t kxA = 0, kxB = 0;     // items finished on tile A / tile B
       bool ok = true;
       auto wait = [&](uint32_t b, uint32_t parity) {
         if (ok && !mbar_wait(b, parity)) {
@@ -309,16 +321,10 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         if (elect_one()) tc_commit(b);
         __syncwarp();
       };
-      // S_t = Q_t K^T of K/V tile gg into tile t's S buffer.  `k_ready`: this thread already
-      // waited for K tile gg (the other tile's S product read it first).
-      auto issue_s = [&](int t, uint32_t gg, bool k_ready) {
-        const int stage = gg % NS;
-        if (!k_ready) {
-          wait(bar(SM::bKFull + stage), (gg / NS) & 1);
-          tc_fence_after();
-        }
+      // S_t = Q_t K^T of K/V tile gg (loaded) into tile t's S buffer, then its commit.
+      auto mma_s = [&](const int t, const uint32_t gg) {
         const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kQTile) >> 4);
-        const uint64_t kd = k_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
+        const uint64_t kd = k_desc0 + ((uint32_t)((gg % NS) * SM::kStageBytes) >> 4);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -327,6 +333,20 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
             tc_mma_ss(tmem + t * 128, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(SM::bSFull + t));
+        }
+        __syncwarp();
+      };
+      // O_t += P_t V with P read from TMEM; `first`: the item's first K/V tile (overwrite O);
+      // `last`: its last one for this tile (commit the final O).
+      auto mma_pv = [&](const int t, const uint64_t vd, const bool first, const bool last) {
+        const uint32_t p_t = tmem + t * 128;
+        const uint32_t o_t = tmem + 256 + t * D;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kChunkKeys / 16; ++kk)
+            tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
+                      (!first || kk > 0) ? 1u : 0u);
+          if (last) tc_commit(bar(SM::bOFinal + t));
         }
         __syncwarp();
       };
@@ -339,46 +359,54 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
         if (item < 0) break;
         const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
-        const int nt_t[2] = {it.nt[0], it.hasB ? it.nt[1] : 0};
+        const int j0 = it.j0, nt_all = it.nt_all;
+        const int ntA = it.nt[0], ntB = it.hasB ? it.nt[1] : 0;
         wait(bar(SM::bQFull), k & 1);
+        wait(bar(SM::bKFull + g % NS), (g / NS) & 1);
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (nt_t[t] > 0) issue_s(t, g, t == 1 && nt_t[0] > 0);
+        mma_s(0, g);
+        if (ntB > 0) mma_s(1, g);
         commit(bar(SM::bKEmpty + g % NS));
-        for (int j = it.j0; j < it.nt_all && ok; ++j) {
-          const uint32_t gj = g + (j - it.j0);
+        for (int j = j0; j < nt_all && ok; ++j) {
+          const uint32_t gj = g + (uint32_t)(j - j0), gn = gj + 1;
           const int stage = gj % NS;
-          wait(bar(SM::bVFull + stage), (gj / NS) & 1);
           const uint64_t vd = v_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
-#pragma unroll 1
-          for (int t = 0; t < 2; ++t) {
-            if (j >= nt_t[t]) continue;
-            const uint32_t tt = gx[t] + (j - it.j0);
-            wait(bar(SM::bPFull + t), tt & 1);
-            if (j == it.j0 && kx[t] > 0) wait(bar(SM::bOFree + t), (kx[t] - 1) & 1);
+          const bool nextA = j + 1 < ntA, nextB = j + 1 < ntB;
+          wait(bar(SM::bVFull + stage), (gj / NS) & 1);
+          if (j < ntA) {
+            wait(bar(SM::bPFull + 0), (gxA + (uint32_t)(j - j0)) & 1);
+            if (j == j0 && kxA > 0) wait(bar(SM::bOFree + 0), (kxA - 1) & 1);
             tc_fence_after();
-            const uint32_t p_t = tmem + t * 128;
-            const uint32_t o_t = tmem + 256 + t * D;
-            if (elect_one()) {
-#pragma unroll
-              for (int kk = 0; kk < kChunkKeys / 16; ++kk)
-                tc_mma_ts(o_t, p_t + kk * 8, vd + ((uint32_t)(kk * 2048) >> 4), idesc_o,
-                          (j > it.j0 || kk > 0) ? 1u : 0u);
-              if (j == nt_t[t] - 1) tc_commit(bar(SM::bOFinal + t));
+            mma_pv(0, vd, j == j0, j == ntA - 1);
+            if (nextA) {
+              wait(bar(SM::bKFull + gn % NS), (gn / NS) & 1);
+              tc_fence_after();
+              mma_s(0, gn);
             }
-            __syncwarp();
-            if (j + 1 < nt_t[t]) issue_s(t, gj + 1, t == 1 && j + 1 < nt_t[0]);
+          }
+          if (j < ntB) {
+            wait(bar(SM::bPFull + 1), (gxB + (uint32_t)(j - j0)) & 1);
+            if (j == j0 && kxB > 0) wait(bar(SM::bOFree + 1), (kxB - 1) & 1);
+            tc_fence_after();
+            mma_pv(1, vd, j == j0, j == ntB - 1);
+            if (nextB) {
+              if (!nextA) {
+                wait(bar(SM::bKFull + gn % NS), (gn / NS) & 1);
+                tc_fence_after();
+              }
+              mma_s(1, gn);
+            }
           }
           commit(bar(SM::bVEmpty + stage));
-          if (j + 1 < it.nt_all) commit(bar(SM::bKEmpty + (gj + 1) % NS));
-          if (j == it.nt_all - 1) commit(bar(SM::bQEmpty));
+          if (j + 1 < nt_all) commit(bar(SM::bKEmpty + gn % NS));
+          if (j == nt_all - 1) commit(bar(SM::bQEmpty));
         }
-        g += it.nt_all - it.j0;
-        for (int t = 0; t < 2; ++t) {
-          if (nt_t[t] > 0) {
-            gx[t] += nt_t[t] - it.j0;
-            kx[t] += 1;
-          }
+        g += (uint32_t)(nt_all - j0);
+        gxA += (uint32_t)(ntA - j0);
+        kxA += 1;
+        if (ntB > 0) {
+          gxB += (uint32_t)(ntB - j0);
+          kxB += 1;
         }
       }
     }
@@ -404,8 +432,11 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       const uint32_t g_item = g;
       g += it.nt_all - it.j0;
       if (t == 1 && !it.hasB) continue;
-      const int nt = it.nt[t];
-      const int diag0 = it.ctx + (it.tok[t] - a.cu_seqlens_q[it.s]);  // row 0's last key
+      const int nt = t ? it.nt[1] : it.nt[0];
+      const int tok = t ? it.tok[1] : it.tok[0];
+      const int rows = t ? it.rows[1] : it.rows[0];
+      const int head = t ? it.head[1] : it.head[0];
+      const int diag0 = it.ctx + (tok - a.cu_seqlens_q[it.s]);  // row 0's last key
       const int limit = diag0 + r;                                     // row r's last key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
@@ -520,8 +551,8 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       __syncwarp();
       tc_fence_after();
       const float inv = 1.f / l_run;
-      const bool store = r < it.rows[t];
-      __nv_bfloat16* orow = outg + ((size_t)(it.tok[t] + r) * a.Hq + it.head[t]) * D;
+      const bool store = r < rows;
+      __nv_bfloat16* orow = outg + ((size_t)(tok + r) * a.Hq + head) * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t ov[32];
@@ -538,7 +569,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         }
       }
       if (store && a.lse != nullptr)
-        a.lse[(size_t)(it.tok[t] + r) * a.Hq + it.head[t]] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        a.lse[(size_t)(tok + r) * a.Hq + head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
       if (r == 0) atomicMax(&hdr->t_pf_end, global_ns());  // role span: last item's end
       tc_fence_before();
       mbar_arrive(bar(SM::bOFree + t));
