@@ -16,8 +16,9 @@
 // per thread slot = the 3 x 168 the launch provides):
 //   warp 0      TMA producer: Q tiles A and B once per item, then the K and V tiles of 128 keys
 //               gathered page run by page run through the block table (staged in shared memory
-//               once per item) into a 2-stage ring (K and V released separately; 128-byte
-//               swizzle, the layout the tensor-core descriptors read directly).
+//               once per item) into a ring of stages, each holding the V tile of one K/V step
+//               and the K tile of the next (128-byte swizzle, the layout the tensor-core
+//               descriptors read directly).
 //   warp 1      tcgen05 issuer (one elected lane of a converged warp): S_t(j) = Q_t K_j^T into
 //               TMEM, and O_t += P_t(j) V_j with P read from TMEM, then at once S_t(j+1); the
 //               other tile's products keep the tensor core busy while a softmax group runs.
@@ -48,13 +49,16 @@ struct PrefillSmem {
   static constexpr int kKVTile = kHalves * kKVHalf;         // one K or V tile
   static constexpr int kStages = (D == 128) ? 2 : 4;
   static constexpr int kQ0 = 0;                             // Q_A, then Q_B
-  static constexpr int kStage0 = 2 * kQTile;                // stage i: K at +0, V at +kKVTile
+  // Ring of kStages slots.  Slot contents for stage m of an item: K tile j0 + m at +0 (m <
+  // the item's K/V tile count) and V tile j0 + m - 1 at +kKVTile (m >= 1): the K tile of the
+  // next S product travels with the V tile of the PV product issued just before it, so one
+  // wait and one release per K/V step cover both.
+  static constexpr int kStage0 = 2 * kQTile;
   static constexpr int kStageBytes = 2 * kKVTile;
   static constexpr int kBar = kStage0 + kStages * kStageBytes;
   // barrier indices (8 bytes each); [2] arrays are indexed by the tile (A = 0, B = 1)
-  static constexpr int bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = bKFull + kStages,
-                       bKEmpty = bVFull + kStages, bVEmpty = bKEmpty + kStages,
-                       bSFull = bVEmpty + kStages, bPFull = bSFull + 2, bOFinal = bPFull + 2,
+  static constexpr int bQFull = 0, bQEmpty = 1, bFull = 2, bEmpty = bFull + kStages,
+                       bSFull = bEmpty + kStages, bPFull = bSFull + 2, bOFinal = bPFull + 2,
                        bOFree = bOFinal + 2, bItemFull = bOFree + 2, bItemEmpty = bItemFull + 2,
                        kNumBars = bItemEmpty + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;         // tmem base, item ids
@@ -162,16 +166,14 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
     mbar_init(bar(SM::bQFull), 1);
     mbar_init(bar(SM::bQEmpty), 1);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(SM::bKFull + i), 1);
-      mbar_init(bar(SM::bVFull + i), 1);
-      mbar_init(bar(SM::bKEmpty + i), 1);
-      mbar_init(bar(SM::bVEmpty + i), 1);
+      mbar_init(bar(SM::bFull + i), 1);
+      mbar_init(bar(SM::bEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SM::bSFull + i), 1);
-      mbar_init(bar(SM::bPFull + i), 128);
+      mbar_init(bar(SM::bPFull + i), 4);   // one arrival per softmax warp
       mbar_init(bar(SM::bOFinal + i), 1);
-      mbar_init(bar(SM::bOFree + i), 128);
+      mbar_init(bar(SM::bOFree + i), 4);
       mbar_init(bar(SM::bItemFull + i), 1);
       mbar_init(bar(SM::bItemEmpty + i), kItemConsumers);
     }
@@ -237,11 +239,10 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
             max(0, min(min((it.nk_all + a.bs - 1) / a.bs, a.max_blocks) - e0, kEntryCache));
         for (int i = lane; i < n_ent; i += 32) ecache[i] = __ldg(row + e0 + i);
         __syncwarp();
-        for (int j = it.j0; j < it.nt_all; ++j, ++g) {
-          const int stage = g % NS;
-          const uint32_t phase = (g / NS) & 1;
+        // Entries of the page runs of K/V tile j (lane = run index mod 32); the previous tile's
+        // are kept for its V tile, which travels one stage later.
+        auto entries = [&](int j, int (&ent)[4]) {
           const int key0 = j * kChunkKeys;
-          int ent[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int sb = p * 32 + lane;
@@ -253,42 +254,56 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
                                           : (lb - e0 < n_ent ? ecache[lb - e0] : __ldg(row + lb));
             }
           }
-          uint32_t nvalid = 0;
+        };
+        // Number of page runs of tile j this warp loads (a run with a bad block id is skipped
+        // and reported).
+        auto count = [&](int j, const int (&ent)[4], bool report_bad) -> uint32_t {
+          uint32_t n = 0;
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int sb = p * 32 + lane;
-            const bool want = sb < nsb && key0 + sb * KB < it.nk_all;
+            const bool want = sb < nsb && j * kChunkKeys + sb * KB < it.nk_all;
             const bool valid = want && ent[p] >= 0 && ent[p] < a.P;
-            if (want && !valid) report(a.err, kErrOutOfRange);
-            nvalid += __popc(__ballot_sync(0xffffffffu, valid));
+            if (report_bad && want && !valid) report(a.err, kErrOutOfRange);
+            n += __popc(__ballot_sync(0xffffffffu, valid));
           }
-          const uint32_t bytes = nvalid * (uint32_t)(SM::kHalves * KB * 128);
+          return n;
+        };
+        auto load = [&](int j, const int (&ent)[4], uint32_t dst, const CUtensorMap* map,
+                        uint32_t full) {
+          const int key0 = j * kChunkKeys;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int sb = p * 32 + lane;
+            const int pos = key0 + sb * KB;
+            if (sb < nsb && pos < it.nk_all && ent[p] >= 0 && ent[p] < a.P) {
+              const int token = ent[p] * a.bs + (pos % a.bs);
+#pragma unroll
+              for (int half = 0; half < SM::kHalves; ++half)
+                tma_load_3d(dst + half * SM::kKVHalf + sb * KB * 128, map, full, half * 64,
+                            it.kvh, token);
+            }
+          }
+        };
+        int ent_k[4] = {-1, -1, -1, -1}, ent_v[4];
+        for (int m = 0; m <= it.nt_all - it.j0; ++m, ++g) {
+          const int j = it.j0 + m;           // K tile of this stage (if j < nt_all)
+          const int stage = g % NS;
+          const uint32_t phase = (g / NS) & 1;
+          const bool has_k = j < it.nt_all, has_v = m > 0;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) ent_v[p] = ent_k[p];   // V of tile j - 1
+          if (has_k) entries(j, ent_k);
+          const uint32_t runs = (has_k ? count(j, ent_k, true) : 0u) + (has_v ? count(j - 1, ent_v, false) : 0u);
           const uint32_t kst = sbase + SM::kStage0 + stage * SM::kStageBytes;
-          const uint32_t vst = kst + SM::kKVTile;
-          // K and V of a stage are released separately: K once both S products of its tile
-          // are done, V once both PV products are.
-#pragma unroll 1
-          for (int kv = 0; kv < 2; ++kv) {
-            if (lane == 0) {
-              if (!mbar_wait(bar((kv ? SM::bVEmpty : SM::bKEmpty) + stage), phase ^ 1))
-                report(a.err, kErrTimeout);
-              mbar_arrive_expect_tx(bar((kv ? SM::bVFull : SM::bKFull) + stage), bytes);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const int sb = p * 32 + lane;
-              const int pos = key0 + sb * KB;
-              if (sb < nsb && pos < it.nk_all && ent[p] >= 0 && ent[p] < a.P) {
-                const int token = ent[p] * a.bs + (pos % a.bs);
-#pragma unroll
-                for (int half = 0; half < SM::kHalves; ++half)
-                  tma_load_3d((kv ? vst : kst) + half * SM::kKVHalf + sb * KB * 128,
-                              kv ? vmap : kmap, bar((kv ? SM::bVFull : SM::bKFull) + stage),
-                              half * 64, it.kvh, token);
-              }
-            }
+          const uint32_t full = bar(SM::bFull + stage);
+          if (lane == 0) {
+            if (!mbar_wait(bar(SM::bEmpty + stage), phase ^ 1)) report(a.err, kErrTimeout);
+            mbar_arrive_expect_tx(full, runs * (uint32_t)(SM::kHalves * KB * 128));
           }
+          __syncwarp();
+          if (has_k) load(j, ent_k, kst, kmap, full);
+          if (has_v) load(j - 1, ent_v, kst + SM::kKVTile, vmap, full);
         }
       }
     } else if (warp == 1) {
@@ -321,10 +336,11 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         if (elect_one()) tc_commit(b);
         __syncwarp();
       };
-      // S_t = Q_t K^T of K/V tile gg (loaded) into tile t's S buffer, then its commit.
-      auto mma_s = [&](const int t, const uint32_t gg) {
+      // S_t = Q_t K^T with the K tile of ring slot `stage` (loaded) into tile t's S buffer,
+      // then its commit.
+      auto mma_s = [&](const int t, const int stage) {
         const uint64_t qd = q_desc0 + ((uint32_t)(t * SM::kQTile) >> 4);
-        const uint64_t kd = k_desc0 + ((uint32_t)((gg % NS) * SM::kStageBytes) >> 4);
+        const uint64_t kd = k_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -361,47 +377,37 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
         const int j0 = it.j0, nt_all = it.nt_all;
         const int ntA = it.nt[0], ntB = it.hasB ? it.nt[1] : 0;
+        // Stage 0 of the item: K tile j0.  (Waiting on a TMA-completed barrier orders the MMAs'
+        // shared-memory reads after the copies; no tensor fence is needed for that.)
         wait(bar(SM::bQFull), k & 1);
-        wait(bar(SM::bKFull + g % NS), (g / NS) & 1);
-        tc_fence_after();
-        mma_s(0, g);
-        if (ntB > 0) mma_s(1, g);
-        commit(bar(SM::bKEmpty + g % NS));
+        wait(bar(SM::bFull + g % NS), (g / NS) & 1);
+        mma_s(0, g % NS);
+        if (ntB > 0) mma_s(1, g % NS);
+        commit(bar(SM::bEmpty + g % NS));
         for (int j = j0; j < nt_all && ok; ++j) {
-          const uint32_t gj = g + (uint32_t)(j - j0), gn = gj + 1;
-          const int stage = gj % NS;
+          // stage j - j0 + 1: V tile j and K tile j + 1
+          const uint32_t gs = g + (uint32_t)(j - j0) + 1;
+          const int stage = gs % NS;
           const uint64_t vd = v_desc0 + ((uint32_t)(stage * SM::kStageBytes) >> 4);
-          const bool nextA = j + 1 < ntA, nextB = j + 1 < ntB;
-          wait(bar(SM::bVFull + stage), (gj / NS) & 1);
+          wait(bar(SM::bFull + stage), (gs / NS) & 1);
           if (j < ntA) {
             wait(bar(SM::bPFull + 0), (gxA + (uint32_t)(j - j0)) & 1);
             if (j == j0 && kxA > 0) wait(bar(SM::bOFree + 0), (kxA - 1) & 1);
             tc_fence_after();
             mma_pv(0, vd, j == j0, j == ntA - 1);
-            if (nextA) {
-              wait(bar(SM::bKFull + gn % NS), (gn / NS) & 1);
-              tc_fence_after();
-              mma_s(0, gn);
-            }
+            if (j + 1 < ntA) mma_s(0, stage);
           }
           if (j < ntB) {
             wait(bar(SM::bPFull + 1), (gxB + (uint32_t)(j - j0)) & 1);
             if (j == j0 && kxB > 0) wait(bar(SM::bOFree + 1), (kxB - 1) & 1);
             tc_fence_after();
             mma_pv(1, vd, j == j0, j == ntB - 1);
-            if (nextB) {
-              if (!nextA) {
-                wait(bar(SM::bKFull + gn % NS), (gn / NS) & 1);
-                tc_fence_after();
-              }
-              mma_s(1, gn);
-            }
+            if (j + 1 < ntB) mma_s(1, stage);
           }
-          commit(bar(SM::bVEmpty + stage));
-          if (j + 1 < nt_all) commit(bar(SM::bKEmpty + gn % NS));
+          commit(bar(SM::bEmpty + stage));
           if (j == nt_all - 1) commit(bar(SM::bQEmpty));
         }
-        g += (uint32_t)(nt_all - j0);
+        g += (uint32_t)(nt_all - j0) + 1;
         gxA += (uint32_t)(ntA - j0);
         kxA += 1;
         if (ntB > 0) {
@@ -430,7 +436,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       if (item < 0) break;
       const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
       const uint32_t g_item = g;
-      g += it.nt_all - it.j0;
+      g += it.nt_all - it.j0 + 1;  // ring stages of the item
       if (t == 1 && !it.hasB) continue;
       const int nt = t ? it.nt[1] : it.nt[0];
       const int tok = t ? it.tok[1] : it.tok[0];
@@ -512,9 +518,9 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
           // product reads them (both groups may do it; they write the same zeros).
           const int first = it.nk_all - key0;  // 1..128
           if (first < kChunkKeys) {
-            const uint32_t gk = g_item + (j - it.j0);
+            const uint32_t gk = g_item + (j - it.j0) + 1;  // the stage holding V tile j
             const int stage = gk % NS;
-            if (!mbar_wait(bar(SM::bVFull + stage), (gk / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
+            if (!mbar_wait(bar(SM::bFull + stage), (gk / NS) & 1)) { report(a.err, kErrTimeout); ok = false; break; }
             const uint32_t vst = sbase + SM::kStage0 + stage * SM::kStageBytes + SM::kKVTile;
             const int nchunks = (kChunkKeys - first) * SM::kHalves * 8;
             for (int i = r; i < nchunks; i += 128) {
@@ -543,7 +549,10 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(SM::bPFull + t));
+        // one arrival per warp once all its lanes have stored P: 4 arrivals on the barrier per
+        // tile instead of 128, which would queue in shared memory behind one another
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(SM::bPFull + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16
@@ -572,7 +581,8 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         a.lse[(size_t)(tok + r) * a.Hq + head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
       if (r == 0) atomicMax(&hdr->t_pf_end, global_ns());  // role span: last item's end
       tc_fence_before();
-      mbar_arrive(bar(SM::bOFree + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SM::bOFree + t));
       gx += nt - it.j0;
       kx += 1;
     }
