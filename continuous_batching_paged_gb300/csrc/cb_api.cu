@@ -270,8 +270,12 @@ static cb_status attention(const void* q, const void* k_pages, const void* v_pag
     return fail(CB_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   const int Hq = dims->num_q_heads, Hkv = dims->num_kv_heads, G = Hq / Hkv;
   if (G > 16) return fail(CB_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
-  if (Hkv > cb::kMaxDecodeHeadsPerCta && Hkv % cb::kMaxDecodeHeadsPerCta != 0)
-    return fail(CB_ERR_UNSUPPORTED, "num_kv_heads > 8 must be a multiple of 8");
+  // KV heads per decode CTA: 8, or 4 when each KV head has more than 8 query heads (two warps
+  // per KV head then share its query heads)
+  const int dec_heads = G > 8 ? cb::kMaxDecodeHeadsPerCta / 2 : cb::kMaxDecodeHeadsPerCta;
+  if (Hkv > dec_heads && Hkv % dec_heads != 0)
+    return fail(CB_ERR_UNSUPPORTED, "num_kv_heads > %d must be a multiple of %d", dec_heads,
+                dec_heads);
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != CB_OK) return st;
@@ -298,7 +302,9 @@ static cb_status attention(const void* q, const void* k_pages, const void* v_pag
   a.KBp = gcd_int(block_size, 128);
   int dctas = options != nullptr ? options->decode_ctas : 0;
   a.decode_auto = dctas <= 0 ? 1 : 0;
-  if (dctas <= 0) dctas = ds->sm_count;
+  const int head_groups = (Hkv + dec_heads - 1) / dec_heads;
+  // by default the decode CTAs of all KV-head groups together take one CTA per SM
+  if (dctas <= 0) dctas = ds->sm_count / head_groups > 0 ? ds->sm_count / head_groups : 1;
   if (dctas > CB_MAX_DECODE_CTAS) dctas = CB_MAX_DECODE_CTAS;
   a.decode_ctas = dctas;
   a.prefill_ctas = ds->sm_count;
@@ -311,7 +317,7 @@ static cb_status attention(const void* q, const void* k_pages, const void* v_pag
   const uint64_t rows = (uint64_t)a.P * (uint64_t)block_size;
   // Decode pass: dims (d, token, head) so one box {64, KB tokens, up to 8 heads} lands in shared
   // memory as [head][token] rows; chunk pass: dims (d, head, token), box {64, 1 head, KBp tokens}.
-  const uint32_t HB = (uint32_t)(Hkv < cb::kMaxDecodeHeadsPerCta ? Hkv : cb::kMaxDecodeHeadsPerCta);
+  const uint32_t HB = (uint32_t)(Hkv < dec_heads ? Hkv : dec_heads);
   if ((st = encode_map(&maps.k_dec, k_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
   if ((st = encode_map(&maps.v_dec, v_pages, D, rows, Hkv, D * 2 * Hkv, D * 2, a.KB, HB)) != CB_OK) return st;
   if ((st = encode_map(&maps.k_chunk, k_pages, D, Hkv, rows, D * 2, D * 2 * Hkv, 1, a.KBp)) != CB_OK) return st;
@@ -342,7 +348,6 @@ static cb_status attention(const void* q, const void* k_pages, const void* v_pag
     if ((e = cb::launch_plan(a, s)) != cudaSuccess) return cuda_fail(e, "plan launch");
   }
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(phase event)");
-  const int head_groups = (Hkv + cb::kMaxDecodeHeadsPerCta - 1) / cb::kMaxDecodeHeadsPerCta;
   if (serial) {
     cb::AttnArgs d = a;
     d.decode_grid = a.decode_ctas * head_groups;

@@ -17,14 +17,14 @@ constexpr int kAttnThreads = kPrefillThreads;
 static_assert(32 * (kMaxDecodeHeadsPerCta + 1) <= kAttnThreads,
               "the decode role fits in the chunk role's CTA");
 
-template <int D>
+template <int D, int QS>
 struct AttnSmem {
-  static constexpr int kTotal = DecodeSmem<D>::kTotal > PrefillSmem<D>::kTotal
-                                    ? DecodeSmem<D>::kTotal
+  static constexpr int kTotal = DecodeSmem<D, QS>::kTotal > PrefillSmem<D>::kTotal
+                                    ? DecodeSmem<D, QS>::kTotal
                                     : PrefillSmem<D>::kTotal;
 };
 
-template <int D, int NTH, bool kWin>
+template <int D, int QS, bool kWin>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap_dec,
@@ -43,23 +43,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + ws_layout(a.S, a.T, a.Hq, a.D).header);
     const bool busy = hdr->dec_tiles > 0;
     if (threadIdx.x == 0 && busy) atomicMin(&hdr->t_dec_start, global_ns());
-    decode_cta<D, NTH>(a, &kmap_dec, &vmap_dec, smem_raw, b % a.decode_ctas, b / a.decode_ctas);
+    decode_cta<D, QS>(a, &kmap_dec, &vmap_dec, smem_raw, b % a.decode_ctas, b / a.decode_ctas);
     if ((threadIdx.x & 31) == 0 && busy) atomicMax(&hdr->t_dec_end, global_ns());
     return;
   }
   prefill_cta<D, kWin>(a, &qmap, &kmap_chunk, &vmap_chunk, smem_raw);
 }
 
-template <int D, int NTH, bool kWin>
+template <int D, int QS, bool kWin>
 static cudaError_t launch_instance(const AttnArgs& a, const AttnMaps& m, cudaStream_t stream) {
-  constexpr int kSmem = AttnSmem<D>::kTotal;
+  constexpr int kSmem = AttnSmem<D, QS>::kTotal;
   // The shared-memory opt-in is a setting of the context: made again whenever the launch
   // goes to another context than the last one configured.
   static unsigned long long configured_ctx = 0;
   const unsigned long long ctx = launch_context_id();
   if (ctx == 0 || configured_ctx != ctx) {
     const cudaError_t e = cudaFuncSetAttribute(
-        attention_kernel<D, NTH, kWin>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        attention_kernel<D, QS, kWin>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured_ctx = ctx;
   }
@@ -76,7 +76,7 @@ static cudaError_t launch_instance(const AttnArgs& a, const AttnMaps& m, cudaStr
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attention_kernel<D, NTH, kWin>, a, m.q, m.k_dec, m.v_dec,
+  return cudaLaunchKernelEx(&cfg, attention_kernel<D, QS, kWin>, a, m.q, m.k_dec, m.v_dec,
                             m.k_chunk, m.v_chunk);
 }
 

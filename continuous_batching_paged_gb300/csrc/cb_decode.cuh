@@ -29,7 +29,16 @@
 
 namespace cb {
 
-constexpr int kDecodeStages = 3;
+// A CTA covers 8 KV heads, one consumer warp per KV head and up to 8 query heads per warp.
+// With more than 8 query heads per KV head (QS = 2) it covers 4 KV heads, two warps per KV
+// head, each taking 8 of its query heads: the same per-warp work as a group of 8.
+template <int QS>
+constexpr int decode_kv_heads() { return kMaxDecodeHeadsPerCta / QS; }
+// Stages of the decode ring, about 192 KB in all: a 16-key stage of K and V is 64 KB at
+// head_dim 128 with 8 KV heads, and proportionally smaller with head_dim 64 or 4 KV heads, so
+// those keep the same bytes in flight per SM with more stages.
+template <int D, int QS>
+constexpr int decode_stages() { return 3 * QS * (128 / D); }
 constexpr uint32_t kInfoFirst = 1u, kInfoLast = 2u, kInfoComplete = 4u;
 
 struct StageInfo {
@@ -43,15 +52,16 @@ struct StageInfo {
   int p0, p1;    // the sequence's tile range [p0, p1) in the concatenated tile order
 };
 
-template <int D>
+template <int D, int QS>
 struct DecodeSmem {
   static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kMaxDecodeHeadsPerCta * kDecodeTileKeys * 128;  // 16 KB
+  static constexpr int kHalfBytes = decode_kv_heads<QS>() * kDecodeTileKeys * 128;  // 16 or 8 KB
   static constexpr int kKVBytes = kHalves * kHalfBytes;                             // K or V
   static constexpr int kStageBytes = 2 * kKVBytes;
-  static constexpr int kBarOffset = kDecodeStages * kStageBytes;
-  static constexpr int kInfoOffset = kBarOffset + 2 * kDecodeStages * 8;
-  static constexpr int kTotal = kInfoOffset + kDecodeStages * (int)sizeof(StageInfo) + 1024;
+  static constexpr int kStages = decode_stages<D, QS>();
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kInfoOffset = kBarOffset + 2 * kStages * 8;
+  static constexpr int kTotal = kInfoOffset + kStages * (int)sizeof(StageInfo) + 1024;
 };
 
 // Largest CTA index c in [0, N) whose range start floor(c * n / N) is <= t.
@@ -157,23 +167,26 @@ __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* par
   }
 }
 
-// Consumer warp of the decode pass: one KV head, its G (<= 8 * NTH) query heads, every tile of
-// the CTA's range.  Products are taken with keys as the m16n8k16 M side and query heads as N:
+// Consumer warp `warp` of the decode pass: KV head warp / QS of the CTA's group, query heads
+// 8 (warp % QS) .. 8 (warp % QS) + 7 of its G (clipped to G), every tile of the CTA's range.  Products are taken with keys as the m16n8k16 M side and query heads as N:
 //   S^T (16 keys x 8 heads)  = K (16 keys x 16 d) . Q^T (16 d x 8 heads), over D/16 k-steps;
 //   O^T (16 d x 8 heads)    += V^T (16 d x 16 keys) . P^T (16 keys x 8 heads), over D/16 m-tiles.
-// P^T is moved from the S^T accumulator layout to the B-operand layout with movmatrix.  With
-// NTH == 1 the warp first loads every K and V fragment of the stage into registers and releases
-// the stage before computing, so the producer refills it sooner.
-template <int D, int NTH>
+// P^T is moved from the S^T accumulator layout to the B-operand layout with movmatrix.  The warp
+// first loads every K and V fragment of the stage into registers and releases the stage before
+// computing, so the producer refills it sooner.
+template <int D, int QS>
 __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase, uint32_t bar_full,
                                                uint32_t bar_empty, const StageInfo* info, int c,
-                                               int hg, int h, long long n_my, long long ntiles,
+                                               int hg, int warp, long long n_my, long long ntiles,
                                                int N, const WsLayout& L, int lane) {
-  using SM = DecodeSmem<D>;
+  using SM = DecodeSmem<D, QS>;
   constexpr int KS = D / 16;  // k-steps of S^T over the head dim
   constexpr int MT = D / 16;  // m-tiles of O^T over the head dim
-  constexpr bool kPreload = (NTH == 1);
-  const int kvh = hg * kMaxDecodeHeadsPerCta + h;  // global KV head
+  constexpr int NTH = 1;      // groups of 8 query heads per warp
+  constexpr bool kPreload = true;
+  const int h = warp / QS;                       // KV head within the CTA's group
+  const int qoff = (warp % QS) * 8;              // first query head (within the KV head's G)
+  const int kvh = hg * decode_kv_heads<QS>() + h;  // global KV head
   const int g = lane >> 2, tq = lane & 3;          // mma fragment coordinates
   float2* part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml);
   float* part_o = reinterpret_cast<float*>(a.ws + L.part_o);
@@ -187,15 +200,15 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
   float mrun[NTH][2], lrun[NTH][2];
   // Stage layout of one 64-wide half of K (or V): runs of KB keys, each run [HB heads][KB keys]
   // of 128-byte rows, so key k of this warp's head is row (k / KB) * HB * KB + h * KB + k % KB.
-  const int KB = a.KB, HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
+  const int KB = a.KB, HB = a.Hkv < decode_kv_heads<QS>() ? a.Hkv : decode_kv_heads<QS>();
   auto row_of = [&](int k) { return (k / KB) * HB * KB + h * KB + (k % KB); };
   // ldmatrix lane -> (key, 16-byte chunk) of the K (non-transposed) and V (transposed) loads
   const int k_row = row_of((lane & 7) + (((lane >> 3) & 1) << 3)), k_csel = lane >> 4;
   const int v_row = row_of((lane & 7) + ((lane >> 4) << 3)), v_csel = (lane >> 3) & 1;
 
   for (long long it = 0; it < n_my; ++it) {
-    const int stage = (int)(it % kDecodeStages);
-    const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+    const int stage = (int)(it % SM::kStages);
+    const uint32_t phase = (uint32_t)((it / SM::kStages) & 1);
     if (!mbar_wait(bar_full + 8 * stage, phase)) {
       report(a.err, kErrTimeout);
       break;
@@ -206,7 +219,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
       for (int ht = 0; ht < NTH; ++ht) {
         mrun[ht][0] = mrun[ht][1] = -INFINITY;
         lrun[ht][0] = lrun[ht][1] = 0.f;
-        const int hl = ht * 8 + g;  // query head within the group held as column g of Q^T
+        const int hl = qoff + ht * 8 + g;  // query head within the group, column g of Q^T
         const uint32_t* qrow = q32 + (((size_t)si.tok * a.Hq + kvh * a.G + hl) * D) / 2;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -343,10 +356,10 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
           la += __shfl_xor_sync(0xffffffffu, la, x);
           lb += __shfl_xor_sync(0xffffffffu, lb, x);
         }
-        const int ha = ht * 8 + 2 * tq, hb = ha + 1;  // query heads (within the group) of my columns
+        const int ha = qoff + ht * 8 + 2 * tq, hb = ha + 1;  // query heads (within the group) of my columns
         if (si.flags & kInfoComplete) {
           const float ia = 1.f / la, ib = 1.f / lb;
-          const int hrow = ht * 8 + g;  // after the transpose a thread holds query head g
+          const int hrow = qoff + ht * 8 + g;  // after the transpose a thread holds query head g
           uint32_t* orow = reinterpret_cast<uint32_t*>(
               outg + ((size_t)si.tok * a.Hq + kvh * a.G + hrow) * D);
 #pragma unroll
@@ -389,7 +402,9 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
         __threadfence();
         __syncwarp();
         int last = 0;
-        if (lane == 0) last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == cl - cf;
+        // QS warps per CTA part finish each (sequence, KV head)
+        if (lane == 0)
+          last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == QS * (cl - cf + 1) - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
@@ -402,7 +417,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
 
 // The producer warp of a decode CTA (see decode_cta): walks the CTA's tile range and issues
 // the TMA copies of every tile's page runs into the stage ring.
-template <int D>
+template <int D, int QS>
 __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensorMap* kmap,
                                                const CUtensorMap* vmap, uint32_t sbase,
                                                uint32_t bar_full, uint32_t bar_empty,
@@ -410,7 +425,7 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
                                                const int32_t* dec_seq, const int32_t* dec_prefix,
                                                const int32_t* cta_first, int c, int hg, int HB,
                                                long long t0, long long t1, int lane) {
-  using SM = DecodeSmem<D>;
+  using SM = DecodeSmem<D, QS>;
     // ===================================================================== producer warp
   if (lane == 0) {
     tma_prefetch_desc(kmap);
@@ -451,8 +466,8 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
       const int nb = (int)((hi - tb) < tiles_per_batch ? (hi - tb) : tiles_per_batch);
       for (int tl = 0; tl < nb; ++tl, ++it) {
         const long long tile = tb + tl;
-        const int stage = (int)(it % kDecodeStages);
-        const uint32_t phase = (uint32_t)((it / kDecodeStages) & 1);
+        const int stage = (int)(it % SM::kStages);
+        const uint32_t phase = (uint32_t)((it / SM::kStages) & 1);
         if (lane == 0 && !mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
           report(a.err, kErrTimeout);
           abort = true;
@@ -492,9 +507,9 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
 #pragma unroll
           for (int half = 0; half < SM::kHalves; ++half) {
             tma_load_3d_hint(kst + half * SM::kHalfBytes + off, kmap, bar_full + 8 * stage,
-                             half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
+                             half * 64, token, hg * decode_kv_heads<QS>(), stream_policy);
             tma_load_3d_hint(vst + half * SM::kHalfBytes + off, vmap, bar_full + 8 * stage,
-                             half * 64, token, hg * kMaxDecodeHeadsPerCta, stream_policy);
+                             half * 64, token, hg * decode_kv_heads<QS>(), stream_policy);
           }
         }
       }
@@ -505,21 +520,22 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
 }
 
 // One CTA of the decode pass: CTA `bx` of the a.decode_ctas CTAs of KV-head group `hg`
-// (8 KV heads per group).  Runs in the attention kernel (cb_attention.cu) with that kernel's
-// dynamic shared memory; uses 32 * (HB + 1) of its threads.
-template <int D, int NTH>
+// (decode_kv_heads<QS>() KV heads per group).  Runs in the attention kernel (cb_attention.cu)
+// with that kernel's dynamic shared memory; uses 32 * (QS * HB + 1) of its threads.
+template <int D, int QS>
 __device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap* kmap,
                                            const CUtensorMap* vmap, uint8_t* smem_raw, int bx,
                                            int hg) {
-  using SM = DecodeSmem<D>;
+  using SM = DecodeSmem<D, QS>;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + SM::kBarOffset;              // kDecodeStages x 8 B
-  const uint32_t bar_empty = bar_full + kDecodeStages * 8;       // kDecodeStages x 8 B
+  const uint32_t bar_full = sbase + SM::kBarOffset;              // kStages x 8 B
+  const uint32_t bar_empty = bar_full + SM::kStages * 8;         // kStages x 8 B
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + SM::kInfoOffset);
 
-  const int HB = a.Hkv < kMaxDecodeHeadsPerCta ? a.Hkv : kMaxDecodeHeadsPerCta;
+  const int HB = a.Hkv < decode_kv_heads<QS>() ? a.Hkv : decode_kv_heads<QS>();
+  const int n_cons = QS * HB;  // consumer warps; the producer is warp n_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
@@ -550,39 +566,24 @@ __device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap*
   if (t0 >= t1) return;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecodeStages; ++i) {
+    for (int i = 0; i < SM::kStages; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, HB);
+      mbar_init(bar_empty + 8 * i, n_cons);
     }
     fence_barrier_init();
   }
   __syncthreads();
 
   auto produce = [&]() {
-    decode_produce<D>(a, kmap, vmap, sbase, bar_full, bar_empty, info, hdr, dec_seq, dec_prefix,
+    decode_produce<D, QS>(a, kmap, vmap, sbase, bar_full, bar_empty, info, hdr, dec_seq, dec_prefix,
                       cta_first, c, hg, HB, t0, t1, lane);
   };
   auto consume = [&]() {
-    decode_consume<D, NTH>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
+    decode_consume<D, QS>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
                            L, lane);
   };
-  if constexpr (NTH == 2) {
-    // Up to 16 query heads per warp need more than the launch's 168 registers per thread:
-    // warpgroups 0 and 1 (the consumers, and the producer when HB < 8) take 200, warpgroup 2
-    // (the producer when HB = 8, and idle warps) gives up to 104; 2 x 128 x 200 + 128 x 104 =
-    // 384 x 168.  Each role runs inside the branch that set its register count.
-    if (warp < 8) {
-      regs_inc<200>();
-      if (warp == HB) produce();
-      else if (warp < HB) consume();
-    } else {
-      regs_dec<104>();
-      if (warp == HB) produce();
-    }
-  } else {
-    if (warp == HB) produce();
-    else if (warp < HB) consume();
-  }
+  if (warp == n_cons) produce();
+  else if (warp < n_cons) consume();
 }
 
 }  // namespace cb

@@ -111,6 +111,18 @@ def test_more_sequences_than_the_planner_keeps_on_chip(cuda_lib):
     _run_full(b)
 
 
+@pytest.mark.parametrize("G,Hkv,ctas", [(12, 4, 0), (16, 8, 0), (16, 8, 3), (16, 2, 64), (9, 8, 0)])
+def test_wide_gqa_groups(cuda_lib, G, Hkv, ctas):
+    # more than 8 query heads per KV head: two decode warps share each KV head's query heads
+    # (4 KV heads per decode CTA, so Hkv = 8 is two head groups); split and whole decode
+    # sequences and a chunk
+    q_lens = [1, 1, 1, 1, 1, 130]
+    kv_lens = [3000, 17, 800, 4096, 1, 130 + 300]
+    b = workloads.build_batch(q_lens, kv_lens, G * Hkv, Hkv, 128, 32, seed=700 + G + Hkv,
+                              name=f"G{G} Hkv{Hkv}")
+    _run_full(b, decode_ctas=ctas)
+
+
 def test_many_kv_heads_two_head_groups(cuda_lib):
     b = workloads.build_batch([1, 1, 70], [300, 45, 170], 32, 16, 128, 16, seed=17,
                               name="Hkv16")
