@@ -384,6 +384,9 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         mma_s(0, g % NS);
         if (ntB > 0) mma_s(1, g % NS);
         commit(bar(SM::bEmpty + g % NS));
+        // Q is read by the S products only: release it once the item's last ones are issued,
+        // so that the next item's Q loads during this item's last K/V step.
+        if (nt_all - j0 == 1) commit(bar(SM::bQEmpty));
         for (int j = j0; j < nt_all && ok; ++j) {
           // stage j - j0 + 1: V tile j and K tile j + 1
           const uint32_t gs = g + (uint32_t)(j - j0) + 1;
@@ -405,7 +408,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
             if (j + 1 < ntB) mma_s(1, stage);
           }
           commit(bar(SM::bEmpty + stage));
-          if (j == nt_all - 1) commit(bar(SM::bQEmpty));
+          if (j == nt_all - 2) commit(bar(SM::bQEmpty));
         }
         g += (uint32_t)(nt_all - j0) + 1;
         gxA += (uint32_t)(ntA - j0);
