@@ -12,8 +12,8 @@
 // so the scheduling is longest-processing-time first and the CTAs working on the heads of one
 // KV group at the same time share its K/V tiles through L2.  Per CTA,
 // warp-specialised (12 warps, three warpgroups; setmaxnreg moves registers from the first
-// warpgroup, which only issues copies and MMAs, to the two softmax warpgroups: 104 + 2 x 200
-// per thread slot = the 3 x 168 the launch provides):
+// warpgroup, which only issues copies and MMAs and claims work, to the two softmax warpgroups:
+// 104 + 2 x 200 per thread slot = the 3 x 168 the launch provides):
 //   warp 0      TMA producer: Q tiles A and B once per item, then the K and V tiles of 128 keys
 //               gathered page run by page run through the block table (staged in shared memory
 //               once per item) into a ring of stages, each holding the V tile of one K/V step
@@ -24,12 +24,16 @@
 //               other tile's products keep the tensor core busy while a softmax group runs.
 //               Completion is signalled with tcgen05.commit on mbarriers.  Also owns the TMEM
 //               allocation.
+//   warp 2      item scheduler: claims the next item from the counter when the producer is
+//               three stages from the end of the current one, decodes it and publishes it in a
+//               shared-memory slot, so that no role starts an item with a chain of global loads.
 //   warps 4-7   softmax group A, warps 8-11 softmax group B: thread r owns query row r (TMEM
 //               lane r) of its tile; it loads its 128 scores with tcgen05.ld, applies the causal
 //               mask only on tiles that cross the diagonal, keeps the running max m and sum l in
 //               registers (tree reductions), writes P (bf16) back over S, rescales O in TMEM
 //               only when m grows by more than 8 in log2 units (otherwise the stale max keeps
-//               every p <= 2^8, exact enough in fp32 and bf16), and writes O / l as bf16.
+//               every p <= 2^8, exact enough in fp32 and bf16), and writes O / l as bf16
+//               through a shared-memory staging buffer (coalesced row stores).
 // TMEM columns: [0,128) S/P of A, [128,256) S/P of B, [256,256+D) O of A, then O of B.
 #pragma once
 
@@ -60,10 +64,20 @@ struct PrefillSmem {
   static constexpr int bQFull = 0, bQEmpty = 1, bFull = 2, bEmpty = bFull + kStages,
                        bSFull = bEmpty + kStages, bPFull = bSFull + 2, bOFinal = bPFull + 2,
                        bOFree = bOFinal + 2, bItemFull = bOFree + 2, bItemEmpty = bItemFull + 2,
-                       kNumBars = bItemEmpty + 2;
-  static constexpr int kMisc = kBar + kNumBars * 8;         // tmem base, item ids
-  static constexpr int kEntries = kMisc + 64;               // block-table row of the item
-  static constexpr int kTotal = kEntries + 4 * kEntryCache + 1024;
+                       bClaim = bItemEmpty + 2, kNumBars = bClaim + 1;
+  static constexpr int kMisc = (kBar + kNumBars * 8 + 127) / 128 * 128;  // tmem base
+  static constexpr int kItems = kMisc + 64;                 // two slots of decoded items
+  static constexpr int kItemSlot = 128;
+  static constexpr int kEntries = kItems + 2 * kItemSlot;   // block-table row of the item
+  // Output staging of the epilogue: per softmax warp 32 rows x 32 columns of bf16 (64 B a row),
+  // so that the output rows leave in coalesced 64-byte runs instead of one 16-byte piece per
+  // row and instruction.
+  static constexpr int kStageOut = kEntries + 4 * kEntryCache;
+  static constexpr int kStageOutWarp = 32 * 64;
+  static constexpr int kTotal = kStageOut + 8 * kStageOutWarp + 1024;
+  // 16-byte vector accesses to the item slots' neighbours and the staging buffer
+  static_assert(kItems % 16 == 0 && kEntries % 16 == 0 && kStageOut % 16 == 0,
+                "shared-memory regions keep 16-byte alignment");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -71,16 +85,19 @@ constexpr int kPrefillThreads = 384;
 constexpr int kRegsIssue = 104;    // warpgroup 0 (producer, MMA issuer, two idle warps)
 constexpr int kRegsSoftmax = 200;  // warpgroups 1 and 2
 static_assert(kRegsIssue + 2 * kRegsSoftmax <= 3 * 168, "register split exceeds the launch");
-constexpr int kItemConsumers = 9;  // MMA thread + 4 warps of each softmax group
+constexpr int kItemConsumers = 10;  // producer, MMA warp, 4 warps of each softmax group
 
 struct PfItem {
+  int item;                                    // claimed item index, -1: no more work
   int s, kvh, ctx;
   int head[2], tok[2], rows[2], nk[2], nt[2];  // per tile: query head, first token, valid rows,
                                                // keys, K/V tiles
+  int qoff[2];                                 // per tile: first query's offset in the chunk
   int nt_all, nk_all;                          // K/V tiles loaded and keys covered for the item
   int j0;                                      // first K/V tile (a sliding window skips older)
-  bool hasB;
+  int hasB;
 };
+static_assert(sizeof(PfItem) <= 128, "a decoded item fits its shared-memory slot");
 
 // Query heads (pairs) per unit: items are unit-major with the head (pair) fastest, so the
 // CTAs on the heads of one KV group at the same time share its K/V tiles through L2.
@@ -93,6 +110,7 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
                                                  const int32_t* pf_seq, const int32_t* pf_prefix,
                                                  const int32_t* pf_order, int n_pf) {
   PfItem it;
+  it.item = item;
   const int hu_n = pf_heads_per_unit(a);
   const int pos = item / hu_n;  // position in the longest-first unit order
   const int hu = item - pos * hu_n;
@@ -123,6 +141,7 @@ __device__ __forceinline__ PfItem pf_decode_item(int item, const AttnArgs& a,
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const bool on = t == 0 || it.hasB;
+    it.qoff[t] = qt[t] * kPrefillTileM;
     it.tok[t] = c0 + qt[t] * kPrefillTileM;
     it.rows[t] = on ? min(kPrefillTileM, q_len - qt[t] * kPrefillTileM) : 0;
     it.nk[t] = on ? it.ctx + qt[t] * kPrefillTileM + it.rows[t] : 0;
@@ -150,7 +169,9 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + SM::kBar + 8 * i; };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + SM::kMisc);
-  volatile int* item_ids = reinterpret_cast<volatile int*>(smem + SM::kMisc + 16);
+  // Decoded items, two slots: the scheduler warp claims and decodes the next item while the
+  // current one runs; every role reads it from here (no global-memory chain at an item's start).
+  auto item_slot = [&](int slot) { return reinterpret_cast<PfItem*>(smem + SM::kItems + slot * SM::kItemSlot); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
@@ -177,6 +198,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       mbar_init(bar(SM::bItemFull + i), 1);
       mbar_init(bar(SM::bItemEmpty + i), kItemConsumers);
     }
+    mbar_init(bar(SM::bClaim), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -204,18 +226,13 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       uint32_t g = 0;
       for (uint32_t k = 0;; ++k) {
         const int slot = k & 1;
-        int item = -1;
-        if (lane == 0) {
-          if (!mbar_wait(bar(SM::bItemEmpty + slot), ((k >> 1) & 1) ^ 1)) report(a.err, kErrTimeout);
-          item = atomicAdd(&hdr->pf_counter, 1);
-          if (item >= n_items) item = -1;
-          if (k == 0 && item >= 0) atomicMin(&hdr->t_pf_start, global_ns());  // role span
-          item_ids[slot] = item;
-          mbar_arrive(bar(SM::bItemFull + slot));
-        }
-        item = __shfl_sync(0xffffffffu, item, 0);
-        if (item < 0) break;
-        const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+        if (!mbar_wait(bar(SM::bItemFull + slot), (k >> 1) & 1)) { report(a.err, kErrTimeout); break; }
+        const PfItem it = *item_slot(slot);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
+        if (it.item < 0) break;
+        // stage at which the scheduler warp is told to claim the next item
+        const int m_claim = max(0, it.nt_all - it.j0 - 3);
         if (lane == 0) {
           if (!mbar_wait(bar(SM::bQEmpty), (k & 1) ^ 1)) report(a.err, kErrTimeout);
           mbar_arrive_expect_tx(bar(SM::bQFull), (it.hasB ? 2 : 1) * SM::kQTile);
@@ -304,7 +321,44 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
           __syncwarp();
           if (has_k) load(j, ent_k, kst, kmap, full);
           if (has_v) load(j - 1, ent_v, kst + SM::kKVTile, vmap, full);
+          // The next item is claimed three stages before this item's last: early enough that
+          // the claim and its decode are done when the item starts, late enough that the claim
+          // order stays the order in which CTAs run out of work (the longest-first schedule
+          // depends on it).
+          if (m == m_claim && lane == 0) mbar_arrive(bar(SM::bClaim));
         }
+      }
+    } else if (warp == 2) {
+      // =================================================================== item scheduler
+      // Claims items from the planner's counter, decodes each into a slot of shared memory
+      // (two slots), and claims the next one when the producer signals that the current
+      // item's loads are near their end.
+      auto claim = [&](uint32_t kc) -> int {
+        const int slot = kc & 1;
+        int item = -1;
+        if (lane == 0) {
+          if (!mbar_wait(bar(SM::bItemEmpty + slot), ((kc >> 1) & 1) ^ 1)) report(a.err, kErrTimeout);
+          item = atomicAdd(&hdr->pf_counter, 1);
+          if (item >= n_items) item = -1;
+          if (kc == 0 && item >= 0) atomicMin(&hdr->t_pf_start, global_ns());  // role span
+        }
+        item = __shfl_sync(0xffffffffu, item, 0);
+        PfItem it;
+        if (item >= 0) it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+        it.item = item;
+        if (lane == 0) {
+          *item_slot(slot) = it;
+          mbar_arrive(bar(SM::bItemFull + slot));
+        }
+        return item;
+      };
+      int item = claim(0);
+      for (uint32_t k = 0; item >= 0; ++k) {
+        if (!mbar_wait(bar(SM::bClaim), k & 1)) {
+          report(a.err, kErrTimeout);
+          break;
+        }
+        item = claim(k + 1);
       }
     } else if (warp == 1) {
       // =================================================================== tcgen05 issuer
@@ -370,11 +424,10 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
         const int slot = k & 1;
         wait(bar(SM::bItemFull + slot), (k >> 1) & 1);
         if (!ok) break;
-        const int item = item_ids[slot];
+        const PfItem it = *item_slot(slot);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
-        if (item < 0) break;
-        const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+        if (it.item < 0) break;
         const int j0 = it.j0, nt_all = it.nt_all;
         const int ntA = it.nt[0], ntB = it.hasB ? it.nt[1] : 0;
         // Stage 0 of the item: K tile j0.  (Waiting on a TMA-completed barrier orders the MMAs'
@@ -433,11 +486,10 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
     for (uint32_t k = 0;; ++k) {
       const int slot = k & 1;
       if (!mbar_wait(bar(SM::bItemFull + slot), (k >> 1) & 1)) { report(a.err, kErrTimeout); break; }
-      const int item = item_ids[slot];
+      const PfItem it = *item_slot(slot);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SM::bItemEmpty + slot));
-      if (item < 0) break;
-      const PfItem it = pf_decode_item<kWin>(item, a, pf_seq, pf_prefix, pf_order, n_pf);
+      if (it.item < 0) break;
       const uint32_t g_item = g;
       g += it.nt_all - it.j0 + 1;  // ring stages of the item
       if (t == 1 && !it.hasB) continue;
@@ -445,7 +497,7 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       const int tok = t ? it.tok[1] : it.tok[0];
       const int rows = t ? it.rows[1] : it.rows[0];
       const int head = t ? it.head[1] : it.head[0];
-      const int diag0 = it.ctx + (tok - a.cu_seqlens_q[it.s]);  // row 0's last key
+      const int diag0 = it.ctx + (t ? it.qoff[1] : it.qoff[0]);  // row 0's last key
       const int limit = diag0 + r;                                     // row r's last key
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
@@ -564,21 +616,41 @@ __device__ __forceinline__ void prefill_cta(const AttnArgs& a, const CUtensorMap
       tc_fence_after();
       const float inv = 1.f / l_run;
       const bool store = r < rows;
-      __nv_bfloat16* orow = outg + ((size_t)(tok + r) * a.Hq + head) * D;
+      // Each 32-column slice of the warp's 32 rows goes through shared memory: lane = row on
+      // the way in (TMEM lane), four lanes per row on the way out, so that every store
+      // instruction writes 64 contiguous bytes of 8 rows.  The 16-byte chunks of a row are
+      // XOR-swizzled by the row pair so that neither side has bank conflicts.
+      const uint32_t stg = sbase + SM::kStageOut + (warp - 4) * SM::kStageOutWarp;
+      const int orow_base = quad * 32;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t ov[32];
         tmem_ld32(t_lane + o_col + ch * 32, ov);
         tc_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[8 * c4 + 2 * i]) * inv,
+                                __uint_as_float(ov[8 * c4 + 2 * i + 1]) * inv);
+          const uint32_t addr = stg + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[0]), "r"(pk[1]),
+                       "r"(pk[2]), "r"(pk[3]) : "memory");
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = (lane >> 2) + 8 * i, c4 = lane & 3;
+          uint4 v;
+          const uint32_t addr = stg + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4);
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+          if (orow_base + row < rows)
+            *reinterpret_cast<uint4*>(outg + ((size_t)(tok + orow_base + row) * a.Hq + head) * D +
+                                      ch * 32 + c4 * 8) = v;
+        }
+        __syncwarp();
       }
       if (store && a.lse != nullptr)
         a.lse[(size_t)(tok + r) * a.Hq + head] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
