@@ -178,6 +178,14 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) at `p` (16-byte aligned) into L2: a hint, no
+// completion to wait for.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // L2 policy for data read once (streamed K/V of decode tokens): its lines are the first to go,
 // so data that other work re-reads stays in L2.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

@@ -11,9 +11,10 @@
 //     results (m, l, o) in the workspace; the last warp to finish a (sequence, KV head) merges
 //     them (an atomic counter per pair decides which): the split-KV scheme with an online
 //     softmax and a log-sum-exp merge, without a separate merge launch.
-//   * One producer warp walks the range, prefetches block-table entries 32 at a time, and
-//     issues TMA tensor copies (128-byte swizzle) of each (page run, KV head, 64-wide half of D)
-//     into a multi-stage shared-memory ring guarded by mbarriers.
+//   * One producer warp walks the range, prefetches block-table entries 32 at a time (and each
+//     sequence's query rows into L2), and issues TMA tensor copies (128-byte swizzle) of each
+//     (page run, KV head, 64-wide half of D) into a multi-stage shared-memory ring guarded by
+//     mbarriers.
 //   * One consumer warp per KV head computes S^T = K Q^T and O^T += V^T P^T for the G query heads
 //     of its group with mma.sync m16n8k16 (bf16 in, fp32 accumulate; keys as the M side, query
 //     heads as N), so the G heads of a GQA group share every K/V byte read from HBM.  It takes
@@ -78,91 +79,78 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
 // and KV head `kvh` (its G query heads): M = max m_c, w_c = 2^(m_c - M),
 // out = sum_c w_c o_c / sum_c w_c l_c, lse = (M + log2 sum_c w_c l_c) * ln 2.
 // Other CTAs wrote these parts: they are read through L2 (ld.global.cg), never from a stale L1
-// line.  Lane i first fetches (m, l) of part-head pair i, so all of them are read in one round
-// trip; then the o rows of 2 heads x 4 parts are loaded together (one vector per lane
-// and row) before any is used, so the merge costs a few L2 round trips, not one per row.
+// line.  Parts are taken kC at a time for kH heads at once, every (m, l) and o row of such a
+// batch loaded before any is used (lane i holds output columns PER i .. PER i + PER - 1), and
+// folded in with a running maximum: one L2 round trip per batch, so a sequence cut in two
+// merges 4 heads in one round trip.
 template <int D>
 __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* part_ml,
                                             const float* part_o, int dec, int tok, int kvh,
                                             int cf, int cl, int lane) {
   constexpr int PER = D / 32;  // output columns per lane: 4 (D = 128) or 2 (D = 64)
-  constexpr int kH = 2, kC = 4;  // heads and parts in flight
+  constexpr int kH = 4, kC = 2;  // heads and parts in flight
   __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
   const int nparts = cl - cf + 1;
-  const bool shfl = nparts <= 32;
-  const int rows_per_round = shfl ? 32 / nparts : a.G;
-  for (int r0 = 0; r0 < a.G; r0 += rows_per_round) {
-    const int rows_here = min(a.G - r0, rows_per_round);
-    const int hr = shfl ? lane / nparts : 0, pc = shfl ? lane % nparts : 0;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (shfl && hr < rows_here)
-      ml = __ldcg(part_ml + ((size_t)(cf + pc) + dec) * a.Hq + kvh * a.G + r0 + hr);
-    // (m, l) of (row rr of this round, part cc): a shuffle, or a load past 32 parts
-    auto part_ml_of = [&](int rr, int cc) -> float2 {
-      if (shfl)
-        return make_float2(__shfl_sync(0xffffffffu, ml.x, rr * nparts + cc),
-                           __shfl_sync(0xffffffffu, ml.y, rr * nparts + cc));
-      return __ldcg(part_ml + ((size_t)(cf + cc) + dec) * a.Hq + kvh * a.G + r0 + rr);
-    };
-    for (int rr0 = 0; rr0 < rows_here; rr0 += kH) {
-      float M[kH], Lsum[kH], acc[kH][PER];
+  for (int r0 = 0; r0 < a.G; r0 += kH) {
+    float M[kH], Lsum[kH], acc[kH][PER];
 #pragma unroll
-      for (int hh = 0; hh < kH; ++hh) {
-        M[hh] = -INFINITY;
-        Lsum[hh] = 0.f;
+    for (int hh = 0; hh < kH; ++hh) {
+      M[hh] = -INFINITY;
+      Lsum[hh] = 0.f;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[hh][i] = 0.f;
-        if (rr0 + hh < rows_here)
-          for (int cc = 0; cc < nparts; ++cc) M[hh] = fmaxf(M[hh], part_ml_of(rr0 + hh, cc).x);
-      }
-      for (int c0 = 0; c0 < nparts; c0 += kC) {
-        float v[kH][kC][PER];
+      for (int i = 0; i < PER; ++i) acc[hh][i] = 0.f;
+    }
+    for (int c0 = 0; c0 < nparts; c0 += kC) {
+      float v[kH][kC][PER];
+      float2 ml[kH][kC];
 #pragma unroll
-        for (int hh = 0; hh < kH; ++hh)
+      for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
-          for (int cc = 0; cc < kC; ++cc) {
-            const int head = kvh * a.G + r0 + rr0 + hh;
-            const float* po =
-                part_o + (((size_t)(cf + c0 + cc) + dec) * a.Hq + head) * D + lane * PER;
-            if (rr0 + hh < rows_here && c0 + cc < nparts) {
-              if constexpr (PER == 4) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(po));
-                v[hh][cc][0] = x.x; v[hh][cc][1] = x.y; v[hh][cc][2] = x.z; v[hh][cc][3] = x.w;
-              } else {
-                const float2 x = __ldcg(reinterpret_cast<const float2*>(po));
-                v[hh][cc][0] = x.x; v[hh][cc][1] = x.y;
-              }
+        for (int cc = 0; cc < kC; ++cc) {
+          const int head = kvh * a.G + r0 + hh;
+          const size_t slot = (size_t)(cf + c0 + cc) + dec;
+          ml[hh][cc] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int i = 0; i < PER; ++i) v[hh][cc][i] = 0.f;
+          if (r0 + hh < a.G && c0 + cc < nparts) {
+            ml[hh][cc] = __ldcg(part_ml + slot * a.Hq + head);
+            const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
+            if constexpr (PER == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(po));
+              v[hh][cc][0] = x.x; v[hh][cc][1] = x.y; v[hh][cc][2] = x.z; v[hh][cc][3] = x.w;
             } else {
-#pragma unroll
-              for (int i = 0; i < PER; ++i) v[hh][cc][i] = 0.f;
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(po));
+              v[hh][cc][0] = x.x; v[hh][cc][1] = x.y;
             }
           }
+        }
 #pragma unroll
-        for (int hh = 0; hh < kH; ++hh)
+      for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
-          for (int cc = 0; cc < kC; ++cc) {
-            if (rr0 + hh < rows_here && c0 + cc < nparts) {
-              const float2 mlx = part_ml_of(rr0 + hh, c0 + cc);
-              const float w = fast_exp2(mlx.x - M[hh]);
-              Lsum[hh] += mlx.y * w;
+        for (int cc = 0; cc < kC; ++cc) {
+          if (r0 + hh < a.G && c0 + cc < nparts) {
+            // every part holds at least one key of its sequence, so its m is finite
+            const float mn = fmaxf(M[hh], ml[hh][cc].x);
+            const float sc = fast_exp2(M[hh] - mn), w = fast_exp2(ml[hh][cc].x - mn);
+            Lsum[hh] = Lsum[hh] * sc + ml[hh][cc].y * w;
 #pragma unroll
-              for (int i = 0; i < PER; ++i) acc[hh][i] += v[hh][cc][i] * w;
-            }
+            for (int i = 0; i < PER; ++i) acc[hh][i] = acc[hh][i] * sc + v[hh][cc][i] * w;
+            M[hh] = mn;
           }
-      }
+        }
+    }
 #pragma unroll
-      for (int hh = 0; hh < kH; ++hh) {
-        if (rr0 + hh >= rows_here) continue;
-        const int head = kvh * a.G + r0 + rr0 + hh;
-        const float inv = 1.f / Lsum[hh];
-        uint32_t* dst =
-            reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
+    for (int hh = 0; hh < kH; ++hh) {
+      if (r0 + hh >= a.G) continue;
+      const int head = kvh * a.G + r0 + hh;
+      const float inv = 1.f / Lsum[hh];
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(outg + ((size_t)tok * a.Hq + head) * D + lane * PER);
 #pragma unroll
-        for (int i = 0; i < PER / 2; ++i)
-          dst[i] = pack_bf16x2(acc[hh][2 * i] * inv, acc[hh][2 * i + 1] * inv);
-        if (lane == 0 && a.lse != nullptr)
-          a.lse[(size_t)tok * a.Hq + head] = (M[hh] + __log2f(Lsum[hh])) * 0.6931471805599453f;
-      }
+      for (int i = 0; i < PER / 2; ++i)
+        dst[i] = pack_bf16x2(acc[hh][2 * i] * inv, acc[hh][2 * i + 1] * inv);
+      if (lane == 0 && a.lse != nullptr)
+        a.lse[(size_t)tok * a.Hq + head] = (M[hh] + __log2f(Lsum[hh])) * 0.6931471805599453f;
     }
   }
 }
@@ -452,6 +440,12 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
     const long long hi = t1 < p1 ? t1 : p1;
     const bool complete = p0 >= t0 && p1 <= t1;
     const int32_t* row = a.block_table + (size_t)s * a.max_blocks;
+    // The consumers read this sequence's query rows (the CTA's head group) at its first tile,
+    // a few stages from now: pull them into L2 so that the read does not wait on HBM.
+    if (lane == 0)
+      l2_prefetch_bulk(static_cast<const __nv_bfloat16*>(a.q) +
+                           ((size_t)tok * a.Hq + (size_t)hg * decode_kv_heads<QS>() * a.G) * D,
+                       (uint32_t)(HB * a.G * D * 2));
     for (long long tb = lo; tb < hi && !abort; tb += tiles_per_batch) {
       // Prefetch the block-table entries of up to 32 (tile, sub-box) pairs.
       int entry = -1;
