@@ -283,6 +283,7 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.ws + L.header);
   int32_t* dec_seq = reinterpret_cast<int32_t*>(a.ws + L.dec_seq);
   int32_t* dec_prefix = reinterpret_cast<int32_t*>(a.ws + L.dec_prefix);
+  int4* dec_rec = reinterpret_cast<int4*>(a.ws + L.dec_rec);
   int32_t* cta_first = reinterpret_cast<int32_t*>(a.ws + L.cta_first);
   int32_t* pf_seq = reinterpret_cast<int32_t*>(a.ws + L.pf_seq);
   int32_t* pf_prefix = reinterpret_cast<int32_t*>(a.ws + L.pf_prefix);
@@ -296,10 +297,12 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   for (int base = 0; base < a.S; base += kPlanThreads) {
     const int s = base + tid;
     int v[4] = {0, 0, 0, 0};
+    int tok = 0, kv = 0;
     if (s < a.S) {
       const int c0 = a.cu_seqlens_q[s], c1 = a.cu_seqlens_q[s + 1];
       const int q_len = c1 - c0;
-      const int kv = a.kv_lens[s];
+      kv = a.kv_lens[s];
+      tok = c0;
       if (s == 0 && c0 != 0) report(a.err, kErrOutOfRange);  // cu_seqlens_q[0] must be 0
       const bool ok = c0 >= 0 && c1 <= a.T && q_len >= 0 && kv >= q_len && kv <= max_kv;
       if (!ok) {
@@ -332,6 +335,7 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
       const int i = carry[0] + ex[0];
       dec_seq[i] = s;
       dec_prefix[i] = carry[1] + ex[1];
+      dec_rec[i] = make_int4(s, tok, kv, carry[1] + ex[1]);
       if (i < kPlanSmemSeqs) s_dec_prefix[i] = carry[1] + ex[1];
     }
     if (v[2]) {
@@ -355,6 +359,7 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   const int n_units = bad ? 0 : carry[3];
   if (tid == 0) {
     dec_prefix[carry[0]] = carry[1];
+    dec_rec[carry[0]] = make_int4(-1, 0, 0, carry[1]);
     pf_prefix[carry[2]] = carry[3];
     if (carry[0] <= kPlanSmemSeqs) s_dec_prefix[carry[0]] = carry[1];
     if (carry[2] <= kPlanSmemSeqs) s_pf_prefix[carry[2]] = carry[3];
@@ -429,15 +434,22 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   // Merge counters of the decode pass: one per (decode sequence, KV head), zero at start.
   int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
   for (int i = tid; i < n_dec * a.Hkv; i += kPlanThreads) merge_cnt[i] = 0;
+  // Indexed by the grid's decode CTA, so that a CTA reads its first sequence in the same round
+  // trip as the plan header.
   const int32_t* dp = n_dec <= kPlanSmemSeqs ? s_dec_prefix : dec_prefix;
-  for (int c = tid; c <= N; c += kPlanThreads) {
-    const long long t0 = ntiles * c / N;
-    int lo = 0, hi = n_dec;  // largest d in [0, n_dec] with dec_prefix[d] <= t0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (dp[mid] <= t0) lo = mid; else hi = mid - 1;
+  for (int bx = tid; bx < a.decode_ctas; bx += kPlanThreads) {
+    const int c = decode_cta_index(bx, N, a.decode_ctas);
+    int lo = -1;
+    if (c >= 0 && c < N) {
+      const long long t0 = ntiles * c / N;
+      lo = 0;
+      int hi = n_dec;  // largest d in [0, n_dec] with dec_prefix[d] <= t0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (dp[mid] <= t0) lo = mid; else hi = mid - 1;
+      }
     }
-    cta_first[c] = lo;
+    cta_first[bx] = lo;
   }
 }
 

@@ -60,8 +60,8 @@ struct PlanHeader {
 
 // Byte offsets of the workspace sections (all 256-byte aligned).
 struct WsLayout {
-  size_t header, dec_seq, dec_prefix, cta_first, pf_seq, pf_prefix, pf_order, merge_cnt, part_ml,
-      part_o, total;
+  size_t header, dec_seq, dec_prefix, dec_rec, cta_first, pf_seq, pf_prefix, pf_order, merge_cnt,
+      part_ml, part_o, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -72,6 +72,10 @@ __host__ __device__ inline WsLayout ws_layout(int S, int T, int Hq, int D) {
   L.header = off;     off = align_up(off + sizeof(PlanHeader), 256);
   L.dec_seq = off;    off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
   L.dec_prefix = off; off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
+  // per decode sequence (sequence, query token, kv_len, first tile) in one 16-byte record, so
+  // that the decode pass gets a sequence's metadata in one load
+  L.dec_rec = off;    off = align_up(off + sizeof(int32_t) * 4 * (size_t)(S + 1), 256);
+  // per decode CTA of the grid: the decode sequence holding its first tile, -1 if it is idle
   L.cta_first = off;  off = align_up(off + sizeof(int32_t) * (size_t)(CB_MAX_DECODE_CTAS + 1), 256);
   L.pf_seq = off;     off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
   L.pf_prefix = off;  off = align_up(off + sizeof(int32_t) * (size_t)(S + 1), 256);
@@ -86,6 +90,24 @@ __host__ __device__ inline WsLayout ws_layout(int S, int T, int Hq, int D) {
 }
 
 #if defined(__CUDACC__)
+
+// Working index of decode CTA bx of a grid of `grid` decode CTAs when N of them work, -1 if bx
+// is idle.  With N below the grid size the working CTAs are spread evenly over the grid, in
+// pairs of consecutive CTAs where N and the grid are even: CTA b (or pair b/2) works when it is
+// the first with its value of floor(b N / grid), and takes that value's range.  The block
+// scheduler puts consecutive CTAs on the two SMs of a TPC and deals TPCs out across the GPCs.
+// Measured beside a chunk pass: with the first N CTAs working the decode pass ran ~6% slower;
+// with single CTAs spread, decode and chunk CTAs shared TPCs and the chunk pass ran ~5% slower;
+// spread pairs ran both at the speed of a launch of exactly N CTAs.
+__device__ __forceinline__ int decode_cta_index(int bx, int N, int grid) {
+  if (N >= grid) return bx;
+  const bool pairs = ((N | grid) & 1) == 0;
+  const int units = pairs ? grid / 2 : grid, wanted = pairs ? N / 2 : N;
+  const int u = pairs ? bx >> 1 : bx;
+  const int cu = (int)((long long)u * wanted / units);
+  if (u > 0 && (long long)(u - 1) * wanted / units == cu) return -1;
+  return pairs ? 2 * cu + (bx & 1) : cu;
+}
 
 __device__ __forceinline__ void report(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 

@@ -410,9 +410,8 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
                                                const CUtensorMap* vmap, uint32_t sbase,
                                                uint32_t bar_full, uint32_t bar_empty,
                                                StageInfo* info, const PlanHeader* hdr,
-                                               const int32_t* dec_seq, const int32_t* dec_prefix,
-                                               const int32_t* cta_first, int c, int hg, int HB,
-                                               long long t0, long long t1, int lane) {
+                                               const int4* dec_rec, int d_first, int c, int hg,
+                                               int HB, long long t0, long long t1, int lane) {
   using SM = DecodeSmem<D, QS>;
     // ===================================================================== producer warp
   if (lane == 0) {
@@ -423,16 +422,16 @@ __device__ __forceinline__ void decode_produce(const AttnArgs& a, const CUtensor
   const int nsb = kDecodeTileKeys / KB;        // page runs (TMA boxes per half and K/V) per tile
   const uint64_t stream_policy = l2_policy_evict_first();  // each K/V row is read once
   const int tiles_per_batch = 32 / nsb;
-  int d = cta_first[c];
+  int d = d_first;
   long long t = t0;
   long long it = 0;
   bool abort = false;
   while (t < t1 && !abort) {
     if (d >= hdr->n_dec) { report(a.err, kErrOutOfRange); break; }
-    const long long p0 = dec_prefix[d], p1 = dec_prefix[d + 1];
-    const int s = dec_seq[d];
-    const int kv = a.kv_lens[s];
-    const int tok = a.cu_seqlens_q[s];
+    // one round trip for the sequence's metadata (the next record's first tile ends its range)
+    const int4 rec = dec_rec[d];
+    const long long p0 = rec.w, p1 = dec_rec[d + 1].w;
+    const int s = rec.x, tok = rec.y, kv = rec.z;
     // with a sliding window the sequence's tiles start at the one holding its first key
     const int lo_key = window_first_key(kv - 1, a.window);
     const int first_tile_key = lo_key / kDecodeTileKeys * kDecodeTileKeys;
@@ -533,29 +532,16 @@ __device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap*
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WsLayout L = ws_layout(a.S, a.T, a.Hq, a.D);
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws + L.header);
-  const int32_t* dec_seq = reinterpret_cast<const int32_t*>(a.ws + L.dec_seq);
-  const int32_t* dec_prefix = reinterpret_cast<const int32_t*>(a.ws + L.dec_prefix);
+  const int4* dec_rec = reinterpret_cast<const int4*>(a.ws + L.dec_rec);
   const int32_t* cta_first = reinterpret_cast<const int32_t*>(a.ws + L.cta_first);
 
+  // The first sequence comes from the planner's per-grid-CTA table, read in the same round trip
+  // as the header (neither depends on the other).
+  const int d_first = cta_first[bx];
   const long long ntiles = hdr->dec_tiles;
   const int N = hdr->decode_ctas;  // planner's CTA count: <= a.decode_ctas, every range non-empty
-  // With N below the grid size the working CTAs are spread evenly over the grid, in pairs of
-  // consecutive CTAs where N and the grid are even: CTA b (or pair b/2) works when it is the
-  // first with its value of floor(b N / grid), and takes that value's range.  The block
-  // scheduler puts consecutive CTAs on the two SMs of a TPC and deals TPCs out across the GPCs.
-  // Measured beside a chunk pass: with the first N CTAs working the decode pass ran ~6% slower;
-  // with single CTAs spread, decode and chunk CTAs shared TPCs and the chunk pass ran ~5%
-  // slower; spread pairs ran both at the speed of a launch of exactly N CTAs.
-  const int grid = a.decode_ctas;
-  int c = bx;
-  if (N < grid) {
-    const bool pairs = ((N | grid) & 1) == 0;
-    const int units = pairs ? grid / 2 : grid, wanted = pairs ? N / 2 : N;
-    const int u = pairs ? bx >> 1 : bx;
-    const int cu = (int)((long long)u * wanted / units);
-    if (u > 0 && (long long)(u - 1) * wanted / units == cu) return;
-    c = pairs ? 2 * cu + (bx & 1) : cu;
-  }
+  const int c = decode_cta_index(bx, N, a.decode_ctas);
+  if (c < 0 || d_first < 0) return;
   const long long t0 = ntiles * c / N, t1 = ntiles * (c + 1) / N;
   if (t0 >= t1) return;
 
@@ -569,8 +555,8 @@ __device__ __forceinline__ void decode_cta(const AttnArgs& a, const CUtensorMap*
   __syncthreads();
 
   auto produce = [&]() {
-    decode_produce<D, QS>(a, kmap, vmap, sbase, bar_full, bar_empty, info, hdr, dec_seq, dec_prefix,
-                      cta_first, c, hg, HB, t0, t1, lane);
+    decode_produce<D, QS>(a, kmap, vmap, sbase, bar_full, bar_empty, info, hdr, dec_rec, d_first,
+                          c, hg, HB, t0, t1, lane);
   };
   auto consume = [&]() {
     decode_consume<D, QS>(a, sbase, bar_full, bar_empty, info, c, hg, warp, t1 - t0, ntiles, N,
