@@ -53,3 +53,32 @@ def test_random_ragged_batch_matches_oracle(cuda_lib, trial):
     ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
                                         b.block_size, b.scale, window=window)
     assert_close(out.float().cpu().numpy(), ref, f"{b.name} (window {window}, fused {fused})")
+
+
+@pytest.mark.parametrize("G", [4, 3])
+def test_many_one_tile_chunk_items(cuda_lib, G):
+    """Hundreds of chunk work items of one K/V tile each (short chunks at short prior contexts,
+    with decodes between them): every chunk CTA runs many items back to back, so the next item
+    is claimed at an item's first stage and the two decoded-item slots turn over quickly.  With
+    an odd group size an item pairs two query tiles of one head; some chunks span two tiles."""
+    rng = np.random.default_rng(9400 + G)
+    q_lens, kv_lens = [], []
+    for i in range(360):
+        if i % 5 == 4:
+            q, ctx = 1, int(rng.integers(1, 200))
+        else:
+            q = int(rng.integers(2, 60)) if i % 7 else int(rng.integers(120, 250))
+            ctx = int(rng.integers(0, 128 - min(q, 127)))
+        q_lens.append(q)
+        kv_lens.append(q + ctx)
+    Hkv = 2
+    b = workloads.build_batch(q_lens, kv_lens, G * Hkv, Hkv, 128, 16, seed=9450 + G,
+                              shuffle_pages=True, name=f"one-tile items G {G}")
+    db = DeviceBatch(b)
+    out = cb.append_attention(db.q, db.k_new, db.v_new, db.k_pages, db.v_pages, db.block_table,
+                              db.cu, db.kv_lens, b.block_size, b.scale)
+    assert cb.get_device_error() == cb.CB_OK
+    kp, vp = oracle_append(b)
+    ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                        b.block_size, b.scale)
+    assert_close(out.float().cpu().numpy(), ref, b.name)
