@@ -82,3 +82,56 @@ def test_many_one_tile_chunk_items(cuda_lib, G):
     ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
                                         b.block_size, b.scale)
     assert_close(out.float().cpu().numpy(), ref, b.name)
+
+
+def _wide_batch(trial):
+    """Wider random mix than _random_batch: GQA groups up to 16 (two warps per KV head in the
+    decode pass), odd groups, block sizes 4-128, explicit decode CTA counts, and every fourth
+    batch hundreds of short sequences (many decode parts and one-tile chunk items)."""
+    rng = np.random.default_rng(77000 + trial)
+    many = trial % 4 == 3
+    S = int(rng.integers(100, 400)) if many else int(rng.integers(1, 60))
+    G = int(rng.choice([1, 2, 3, 4, 8, 12, 16]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    if G > 8:
+        Hkv = min(Hkv, 4)
+    D = int(rng.choice([64, 128]))
+    bs = int(rng.choice([4, 8, 16, 32, 64, 128]))
+    q_lens, kv_lens = [], []
+    for _ in range(S):
+        u = rng.random()
+        if many:
+            q = 1 if u < 0.3 else int(rng.integers(2, 80))
+            ctx = int(rng.integers(0, 200))
+        else:
+            q = 0 if u < 0.05 else 1 if u < 0.55 else int(rng.integers(2, 400))
+            ctx = int(rng.integers(0, 3000))
+        q_lens.append(q)
+        kv_lens.append(max(q + ctx, 1) if q == 0 else q + ctx)
+    window = int(rng.choice([0, 0, 0, 0, 32, 200, 1000]))
+    decode_ctas = int(rng.choice([0, 0, 0, 1, 5, 40, 200]))
+    fused = bool(rng.integers(0, 2))
+    b = workloads.build_batch(q_lens, kv_lens, G * Hkv, Hkv, D, bs, seed=78000 + trial,
+                              shuffle_pages=True, name=f"wide random {trial}")
+    return b, window, decode_ctas, fused
+
+
+@pytest.mark.parametrize("trial", range(24))
+def test_wide_random_batch_matches_oracle(cuda_lib, trial):
+    b, window, decode_ctas, fused = _wide_batch(trial)
+    db = DeviceBatch(b)
+    kw = dict(window=window, decode_ctas=decode_ctas)
+    if fused:
+        out = cb.append_attention(db.q, db.k_new, db.v_new, db.k_pages, db.v_pages,
+                                  db.block_table, db.cu, db.kv_lens, b.block_size, b.scale, **kw)
+    else:
+        db.append()
+        out = cb.ragged_paged_attention(db.q, db.k_pages, db.v_pages, db.block_table, db.cu,
+                                        db.kv_lens, b.block_size, b.scale, **kw)
+    assert cb.get_device_error() == cb.CB_OK
+    kp, vp = oracle_append(b)
+    assert np.array_equal(bits_of(db.k_pages), kp) and np.array_equal(bits_of(db.v_pages), vp)
+    ref, _ = opa.ragged_paged_attention(b.q, kp, vp, b.block_table, b.cu_seqlens_q, b.kv_lens,
+                                        b.block_size, b.scale, window=window)
+    assert_close(out.float().cpu().numpy(), ref,
+                 f"{b.name} (window {window}, decode_ctas {decode_ctas}, fused {fused})")
