@@ -433,7 +433,9 @@ __device__ __forceinline__ void plan_cta(const AttnArgs& a) {
   const int N = s_N;
   // Merge counters of the decode pass: one per (decode sequence, KV head), zero at start.
   int32_t* merge_cnt = reinterpret_cast<int32_t*>(a.ws + L.merge_cnt);
-  for (int i = tid; i < n_dec * a.Hkv; i += kPlanThreads) merge_cnt[i] = 0;
+  // (one per decode sequence, KV head and group of 8 query heads: two groups when G > 8)
+  const int head_groups = a.G > 8 ? 2 : 1;
+  for (int i = tid; i < n_dec * a.Hkv * head_groups; i += kPlanThreads) merge_cnt[i] = 0;
   // Indexed by the grid's decode CTA, so that a CTA reads its first sequence in the same round
   // trip as the plan header.
   const int32_t* dp = n_dec <= kPlanSmemSeqs ? s_dec_prefix : dec_prefix;

@@ -8,8 +8,8 @@
 //     N equal contiguous ranges (N from the planner, at most `decode_ctas`), one per working
 //     CTA: every CTA streams the same number of bytes whatever the length mix.  The CTAs are
 //     the first CTAs of the attention kernel (cb_attention.cu); the chunk pass's CTAs follow.  A sequence cut by range boundaries leaves per-CTA partial
-//     results (m, l, o) in the workspace; the last warp to finish a (sequence, KV head) merges
-//     them (an atomic counter per pair decides which): the split-KV scheme with an online
+//     results (m, l, o) in the workspace; the last warp to finish a (sequence, KV head, group of
+//     8 query heads) merges them (an atomic counter per triple decides which): the split-KV scheme with an online
 //     softmax and a log-sum-exp merge, without a separate merge launch.
 //   * One producer warp walks the range, prefetches block-table entries 32 at a time (and each
 //     sequence's query rows into L2), and issues TMA tensor copies (128-byte swizzle) of each
@@ -76,7 +76,7 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
 }
 
 // One warp combines the partial (m, l, o) that CTAs cf..cl wrote for decode sequence `dec`
-// and KV head `kvh` (its G query heads): M = max m_c, w_c = 2^(m_c - M),
+// and query heads h0 .. h1 - 1 of KV head `kvh`'s group: M = max m_c, w_c = 2^(m_c - M),
 // out = sum_c w_c o_c / sum_c w_c l_c, lse = (M + log2 sum_c w_c l_c) * ln 2.
 // Other CTAs wrote these parts: they are read through L2 (ld.global.cg), never from a stale L1
 // line.  Parts are taken kC at a time for kH heads at once, every (m, l) and o row of such a
@@ -86,12 +86,12 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long n, int N) {
 template <int D>
 __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* part_ml,
                                             const float* part_o, int dec, int tok, int kvh,
-                                            int cf, int cl, int lane) {
+                                            int cf, int cl, int h0, int h1, int lane) {
   constexpr int PER = D / 32;  // output columns per lane: 4 (D = 128) or 2 (D = 64)
   constexpr int kH = 4, kC = 2;  // heads and parts in flight
   __nv_bfloat16* outg = static_cast<__nv_bfloat16*>(a.out);
   const int nparts = cl - cf + 1;
-  for (int r0 = 0; r0 < a.G; r0 += kH) {
+  for (int r0 = h0; r0 < h1; r0 += kH) {
     float M[kH], Lsum[kH], acc[kH][PER];
 #pragma unroll
     for (int hh = 0; hh < kH; ++hh) {
@@ -112,7 +112,7 @@ __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* par
           ml[hh][cc] = make_float2(-INFINITY, 0.f);
 #pragma unroll
           for (int i = 0; i < PER; ++i) v[hh][cc][i] = 0.f;
-          if (r0 + hh < a.G && c0 + cc < nparts) {
+          if (r0 + hh < h1 && c0 + cc < nparts) {
             ml[hh][cc] = __ldcg(part_ml + slot * a.Hq + head);
             const float* po = part_o + (slot * a.Hq + head) * D + lane * PER;
             if constexpr (PER == 4) {
@@ -128,7 +128,7 @@ __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* par
       for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
         for (int cc = 0; cc < kC; ++cc) {
-          if (r0 + hh < a.G && c0 + cc < nparts) {
+          if (r0 + hh < h1 && c0 + cc < nparts) {
             // every part holds at least one key of its sequence, so its m is finite
             const float mn = fmaxf(M[hh], ml[hh][cc].x);
             const float sc = fast_exp2(M[hh] - mn), w = fast_exp2(ml[hh][cc].x - mn);
@@ -141,7 +141,7 @@ __device__ __forceinline__ void merge_parts(const AttnArgs& a, const float2* par
     }
 #pragma unroll
     for (int hh = 0; hh < kH; ++hh) {
-      if (r0 + hh >= a.G) continue;
+      if (r0 + hh >= h1) continue;
       const int head = kvh * a.G + r0 + hh;
       const float inv = 1.f / Lsum[hh];
       uint32_t* dst =
@@ -385,18 +385,22 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
         }
       }
       if (!(si.flags & kInfoComplete)) {
-        // Split sequence: the last warp to finish this (sequence, KV head) merges all parts.
+        // Split sequence: the last warp to finish this (sequence, KV head, group of 8 query
+        // heads) merges the group's parts.
         const int cf = cta_of_tile(si.p0, ntiles, N), cl = cta_of_tile(si.p1 - 1, ntiles, N);
         __threadfence();
         __syncwarp();
         int last = 0;
-        // QS warps per CTA part finish each (sequence, KV head)
+        // one counter per (sequence, KV head, group of 8 query heads): with QS warps per KV
+        // head, the last warp of each group merges that group's heads, the groups in parallel
         if (lane == 0)
-          last = atomicAdd(merge_cnt + (size_t)si.dec * a.Hkv + kvh, 1) == QS * (cl - cf + 1) - 1;
+          last = atomicAdd(merge_cnt + ((size_t)si.dec * a.Hkv + kvh) * QS + warp % QS, 1) ==
+                 cl - cf;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, lane);
+          merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, qoff,
+                         qoff + 8 < a.G ? qoff + 8 : a.G, lane);
         }
       }
     }
