@@ -221,6 +221,7 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
     const uint32_t kst = sbase + stage * SM::kStageBytes;
     const uint32_t vst = kst + SM::kKVBytes;
     const bool tail = si.key0 + kDecodeTileKeys > si.kv;
+
     const bool head = si.key0 < si.lo;  // keys before the sliding window in this tile
 
     // ---- K fragments (A operand of S^T: rows = keys, k = head dim)
@@ -336,6 +337,15 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
     }
 
     if (si.flags & kInfoLast) {
+      // A split part: read its counter now (acquire), so that the value is in by the time the
+      // part is written.  If every other part has counted already, this warp is the last and
+      // merges without an atomic of its own.
+      int peek = -1;
+      if (!(si.flags & kInfoComplete) && lane == 0)
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];"
+                     : "=r"(peek)
+                     : "l"(merge_cnt + ((size_t)si.dec * a.Hkv + kvh) * QS + warp % QS)
+                     : "memory");
 #pragma unroll
       for (int ht = 0; ht < NTH; ++ht) {
         float la = lrun[ht][0], lb = lrun[ht][1];
@@ -388,20 +398,26 @@ __device__ __forceinline__ void decode_consume(const AttnArgs& a, uint32_t sbase
         // Split sequence: the last warp to finish this (sequence, KV head, group of 8 query
         // heads) merges the group's parts.
         const int cf = cta_of_tile(si.p0, ntiles, N), cl = cta_of_tile(si.p1 - 1, ntiles, N);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
         // one counter per (sequence, KV head, group of 8 query heads): with QS warps per KV
-        // head, the last warp of each group merges that group's heads, the groups in parallel
-        if (lane == 0)
-          last = atomicAdd(merge_cnt + ((size_t)si.dec * a.Hkv + kvh) * QS + warp % QS, 1) ==
-                 cl - cf;
-        last = __shfl_sync(0xffffffffu, last, 0);
+        // head, the last warp of each group merges that group's heads, the groups in parallel.
+        // Counts only grow, so a counter already at parts - 1 leaves this warp the last (the
+        // fence makes its own part, read back through L2, visible to all its lanes).
+        int last = __shfl_sync(0xffffffffu, peek, 0) == cl - cf ? 1 : 0;
         if (last) {
           __threadfence();
+          __syncwarp();
+        } else {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0)
+            last = atomicAdd(merge_cnt + ((size_t)si.dec * a.Hkv + kvh) * QS + warp % QS, 1) ==
+                   cl - cf;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) __threadfence();
+        }
+        if (last)
           merge_parts<D>(a, part_ml, part_o, si.dec, si.tok, kvh, cf, cl, qoff,
                          qoff + 8 < a.G ? qoff + 8 : a.G, lane);
-        }
       }
     }
   }
